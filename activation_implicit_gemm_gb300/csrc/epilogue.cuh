@@ -1,0 +1,53 @@
+// Fused epilogue math shared by every kernel of the library: the activation of a
+// pre-activation value v = acc + B[m] + Z[n,m,o], computed in fp32 (README
+// "Attributes": the activation list and activation_params). The one rounding to T
+// happens after the activation, as the f16 subgroup-matrix variants of the package
+// describe it (f32 accumulation, then bias, residual, activation and f16 rounding).
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "fconv_internal.h"
+
+namespace fconv {
+
+__device__ __forceinline__ float gelu_tanh_f(float v) {
+  const float k = 0.7978845608028654f;  // sqrt(2/pi)
+  return 0.5f * v * (1.0f + tanhf(k * (v + 0.044715f * v * v * v)));
+}
+
+// act(v) for the activation ids of fconv_act; alpha/beta are the resolved parameters.
+__device__ __forceinline__ float apply_act(int act, float v, float alpha, float beta) {
+  switch (act) {
+    case FCONV_ACT_NONE: return v;
+    case FCONV_ACT_RELU: return fmaxf(v, 0.0f);
+    case FCONV_ACT_LEAKYRELU: return v < 0.0f ? alpha * v : v;
+    case FCONV_ACT_SIGMOID: return 1.0f / (1.0f + expf(-v));
+    case FCONV_ACT_TANH: return tanhf(v);
+    case FCONV_ACT_HARDSIGMOID: return fminf(fmaxf(alpha * v + beta, 0.0f), 1.0f);
+    case FCONV_ACT_HARDSWISH: return v * fminf(fmaxf(v * (1.0f / 6.0f) + 0.5f, 0.0f), 1.0f);
+    case FCONV_ACT_CLIP: return fminf(fmaxf(v, alpha), beta);
+    case FCONV_ACT_QUICKGELU: return v / (1.0f + expf(-alpha * v));
+    case FCONV_ACT_ELU: return v > 0.0f ? v : alpha * expm1f(v);
+    case FCONV_ACT_GELU:
+      if (alpha != 0.0f) return gelu_tanh_f(v);
+      return 0.5f * v * (1.0f + erff(v * 0.7071067811865476f));
+    case FCONV_ACT_FASTGELU: return gelu_tanh_f(v);
+    case FCONV_ACT_SOFTPLUS: return fmaxf(v, 0.0f) + log1pf(expf(-fabsf(v)));
+    case FCONV_ACT_THRESHOLDEDRELU: return v > alpha ? v : 0.0f;
+    case FCONV_ACT_ERF: return erff(v);
+    default: return v;
+  }
+}
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float v) {
+  return __float2half_rn(v);
+}
+
+}  // namespace fconv

@@ -1,0 +1,61 @@
+// Internal interface between the planner (fconv_api.cpp) and the CUDA launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/fconv.h"
+
+namespace fconv {
+
+// Resolved geometry of one FusedConv call. Spatial axes are (depth, height, width);
+// axes the rank lacks have extent 1, stride 1, dilation 1 and pad 0. Pads are the
+// begin pads actually applied (manifest derive effectivePadFront/Top/Left).
+struct ConvGeom {
+  int dtype;                    // fconv_dtype
+  int N, C, M, G, Cg, Mg;
+  int ID, IH, IW;
+  int OD, OH, OW;
+  int KD, KH, KW;
+  int sD, sH, sW;
+  int dD, dH, dW;
+  int pD, pH, pW;
+  int act;                      // fconv_act
+  float alpha, beta;            // resolved activation parameters
+  int has_bias, has_z;
+  long long P;                  // OD*OH*OW
+  long long IS;                 // ID*IH*IW
+  int KV;                       // KD*KH*KW
+  int Kg;                       // Cg*KV
+};
+
+struct ConvArgs {
+  const void* x;
+  const void* w;
+  const void* b;
+  const void* z;
+  void* y;
+  void* ws;
+};
+
+// Tensor-core implicit GEMM configuration.
+struct IgemmConfig {
+  int tile_n;      // MMA N (channels per tile): 16..256, multiple of 16
+  int split_k;     // number of K splits (>= 1)
+  int stages;      // shared-memory pipeline depth
+};
+
+// Launchers: return cudaError_t as int (0 = success).
+int launch_direct(const ConvGeom& g, const ConvArgs& a, void* stream);
+int launch_depthwise(const ConvGeom& g, const ConvArgs& a, void* stream);
+int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, void* stream);
+bool igemm_tc_supported(const ConvGeom& g);
+bool depthwise_supported(const ConvGeom& g);
+int igemm_tc_stages(int tile_n);
+size_t igemm_tc_smem_bytes(int tile_n, int stages);
+size_t igemm_tc_workspace_bytes(const ConvGeom& g, const IgemmConfig& c);
+
+// Device error word (set by kernels whose bounded waits gave up). Reads and clears.
+int read_and_clear_device_error(void* stream, unsigned* value);
+
+}  // namespace fconv
