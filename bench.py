@@ -1,0 +1,396 @@
+"""FusedConv benchmark: one JSON line on stdout.
+
+A step is one pass of the whole FusedConv suite: the eleven synthetic convolutions of
+the five benchmark workloads (2-D fp32 3->8; 1-D fp16 dilated SAME_UPPER +B+Z; the
+fp16 residual-CNN 3x3 stack at batch 512; the fp16 vision-encoder stem patch-embed,
+depthwise 7x7 and strided downsample; the fp16 3-D strided SAME_LOWER conv, dense and
+grouped), each auto-planned by the library exactly as a user call would be. Inputs are
+resident in HBM; L2 is flushed (a 256 MiB memset) before every step, outside the timed
+events. `value` = algorithmic FLOPs of all ranks / the max over ranks of the device time.
+
+Also reported: per-conv TFLOP/s, GB/s and roofline fractions (CUDA events around every
+conv launch on the launching stream), the roofline of the dominant launch, the
+end-to-end throughput through the public API with pinned host buffers (H2D of every
+input and D2H of every output inside the timed region), the CPU oracle's throughput on
+the host cores, and SM clocks sampled during the timed region.
+
+`--impl reference` times the CPU oracle (the only reference this operator has) on the
+host cores, on bounded batch-1 samples of the same convolutions.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "FusedConv TFLOP/s (fp16/fp32) and % of roofline per config; depthwise GB/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples with host timestamps."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        win = [p for (t, p) in self.samples if t0 <= t <= t1]
+        if not win:
+            win = [p for (_, p) in self.samples]
+        if not win:
+            return None
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in win if num(p[1]) is not None]
+        mx = [num(p[2]) for p in win if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in win for i in range(4) if p[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(win)}
+
+
+def conv_tensors(case):
+    import oracle
+    ys = oracle.output_shape(case.x_shape, case.w_shape, **case.attrs())
+    return workloads.make_inputs(case, ys), ys
+
+
+def bound_of(flops, bytes_, peaks):
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    return "tensor" if flops / bytes_ >= ridge else "hbm"
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    ws_n, rank, local = dist_env()
+    if ws_n > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import activation_implicit_gemm_gb300 as fc
+    from activation_implicit_gemm_gb300 import _lib
+    fc.build()
+    peaks, peaks_kind = load_peaks()
+
+    convs = []
+    for case in workloads.ALL_CASES:
+        t, ys = conv_tensors(case)
+        dt = _lib.F16 if case.dtype == "f16" else _lib.F32
+        plan = fc.FusedConvPlan(dt, case.x_shape, case.w_shape, has_bias=case.has_bias,
+                                has_z=case.has_z, device=local, **case.attrs())
+        d = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).to(dev))
+             for k, v in t.items()}
+        h = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).pin_memory())
+             for k, v in t.items()}
+        tdt = torch.float16 if case.dtype == "f16" else torch.float32
+        y = torch.empty(plan.y_shape, dtype=tdt, device=dev)
+        yh = torch.empty(plan.y_shape, dtype=tdt).pin_memory()
+        wsb = (torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+               if plan.workspace_bytes else None)
+        convs.append(dict(case=case, plan=plan, d=d, h=h, y=y, yh=yh, ws=wsb))
+    total_flops = sum(c["plan"].flops for c in convs)
+    launches_per_step = sum(1 + (1 if c["plan"].split_k > 1 else 0) for c in convs)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        for i, c in enumerate(convs):
+            if evs is not None:
+                evs[i].record(stream)
+            d = c["d"]
+            c["plan"].run(d["x"], d["w"], d["b"], d["z"], y=c["y"], workspace=c["ws"],
+                          stream=stream)
+        if evs is not None:
+            evs[len(convs)].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(convs) + 1)]
+          for _ in range(K)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if ws_n > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_host0 = time.time()
+    for k in range(K):
+        flush.zero_()
+        step(ev[k])
+    torch.cuda.synchronize()
+    if ws_n > 1:
+        dist.barrier()
+    t_host1 = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+    clocks = sampler.summary(t_host0, t_host1)
+
+    per_conv_ms = [0.0] * len(convs)
+    step_ms = []
+    for k in range(K):
+        s = 0.0
+        for i in range(len(convs)):
+            dt_ms = ev[k][i].elapsed_time(ev[k][i + 1])
+            per_conv_ms[i] += dt_ms
+            s += dt_ms
+        step_ms.append(s)
+    dev_ms = sum(step_ms)
+    if ws_n > 1:
+        tt = torch.tensor([dev_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        dev_ms = float(tt.item())
+    ms_per_step = dev_ms / K
+    value = total_flops * ws_n * K / (dev_ms * 1e-3) / 1e12
+
+    # per-conv breakdown and the dominant launch's roofline
+    per = []
+    for i, c in enumerate(convs):
+        p = c["plan"]
+        ms = per_conv_ms[i] / K
+        fl, by = p.flops, p.bytes
+        bnd = bound_of(fl, by, peaks)
+        tf = fl / (ms * 1e-3) / 1e12
+        gbs = by / (ms * 1e-3) / 1e9
+        if bnd == "tensor":
+            frac = tf / peaks["bf16_tflops"]
+        else:
+            frac = gbs / peaks["hbm_gbs"]
+        attain = min(peaks["bf16_tflops"] * 1e12, fl / by * peaks["hbm_gbs"] * 1e9) / 1e12
+        per.append({"conv": c["case"].name, "route": p.route, "tile_n": p.tile_n,
+                    "split_k": p.split_k, "us": round(ms * 1e3, 2), "tflops": round(tf, 2),
+                    "gbs": round(gbs, 1), "bound": bnd, "frac_of_bound": round(frac, 4),
+                    "frac_of_fp16_peak": round(tf / peaks["bf16_tflops"], 4),
+                    "frac_of_attainable": round(tf / attain, 4)})
+    top = max(range(len(convs)), key=lambda i: per_conv_ms[i])
+    tp = convs[top]["plan"]
+    tms = per_conv_ms[top] / K
+    tb = bound_of(tp.flops, tp.bytes, peaks)
+    if tb == "tensor":
+        ach, pk, unit = tp.flops / (tms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        ach, pk, unit = tp.bytes / (tms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+    traffic = load_traffic(convs[top]["case"].name)
+    roofline = {"bound": tb, "achieved": round(ach, 3), "peak": pk, "unit": unit,
+                "frac": round(ach / pk, 4), "traffic": traffic,
+                "kernel": {"igemm_tc": "igemm_tc_kernel", "depthwise": "dw_kernel_fast",
+                           "direct": "direct_conv_kernel"}[tp.route],
+                "launch": convs[top]["case"].name, "peak_kind": f"{peaks_kind} (burst)",
+                "algorithmic_flops_per_launch": tp.flops,
+                "algorithmic_bytes_per_launch": tp.bytes}
+
+    # end to end through the public API with pinned host buffers
+    e2e_steps = max(3, min(20, K))
+    h2d = sum(sum(v.numel() * v.element_size() for v in c["h"].values() if v is not None)
+              for c in convs)
+    d2h = sum(c["yh"].numel() * c["yh"].element_size() for c in convs)
+
+    def e2e_step():
+        for c in convs:
+            d, hh = c["d"], c["h"]
+            for key in ("x", "w", "b", "z"):
+                if hh[key] is not None:
+                    d[key].copy_(hh[key], non_blocking=True)
+            c["plan"].run(d["x"], d["w"], d["b"], d["z"], y=c["y"], workspace=c["ws"],
+                          stream=stream)
+            c["yh"].copy_(c["y"], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if ws_n > 1:
+        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = total_flops * ws_n * e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+    out = {"metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws_n,
+           "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+           "data": "synthetic (seeded splitmix64/Box-Muller inputs of the benchmark shapes)",
+           "config": {"workload": "fusedconv_suite: 11 convs of the 5 benchmark workloads "
+                                  "(2-D fp32 3->8 k3; 1-D fp16 64->64 k5 d2 SAME_UPPER +B+Z; "
+                                  "3x3 CNN stack N=512 3->64@32, 64->128@16 +Z, 128->256@8, "
+                                  "256->512@4 +Z QuickGelu; stem patch k7 s4 +B Gelu, "
+                                  "depthwise k7 +B+Z Clip, downsample k2 s2; 3-D k3 s2 "
+                                  "SAME_LOWER +B HardSwish, dense and group 4 +Z)",
+                      "flops_per_step": total_flops, "l2": "flushed before every step "
+                      "(256 MiB memset outside the timed events)",
+                      "parallelism": f"replicas x{ws_n} (no data-path collective)",
+                      "fp32_convs": "the 2-D 3->8 conv computes in fp32"},
+           "per_conv": per, "roofline": roofline,
+           "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s",
+                   "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                   "steps": e2e_steps, "api": "FusedConvPlan.run (C ABI fconv_run)"},
+           "gpu_launches": launches_per_step * K, "clocks": clocks}
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if ws_n > 1:
+        dist.destroy_process_group()
+
+
+def load_traffic(conv_name):
+    """DRAM bytes per launch from a committed ncu summary, when one matches this conv."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    return d.get(conv_name)
+
+
+def cpu_baseline():
+    """The oracle, as it stands, on the host cores over the whole suite (one pass)."""
+    import oracle
+    flops = 0.0
+    secs = 0.0
+    for case in workloads.ALL_CASES:
+        t, _ = conv_tensors(case)
+        t0 = time.perf_counter()
+        y, _ = oracle.fused_conv(t["x"], t["w"], t["b"], t["z"], **case.attrs())
+        secs += time.perf_counter() - t0
+        flops += 2.0 * y.size * np.prod(case.w_shape[1:])
+        if secs > 60.0:
+            break
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s",
+            "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"one pass over the suite's convolutions at full size "
+                      f"({flops / 1e9:.1f} GFLOP, {secs:.1f} s, fp64 direct loops, OpenMP)"}
+
+
+def run_reference(args):
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    cases = workloads.ALL_CASES
+    samples = []
+    for case in cases:
+        ys = oracle.output_shape(case.x_shape, case.w_shape, **case.attrs())
+        t = workloads.make_inputs(case, ys, batch=1)
+        samples.append((case, t))
+    flops = 0.0
+    secs = 0.0
+    for k in range(args.warmup + args.steps):
+        case, t = samples[k % len(samples)]
+        t0 = time.perf_counter()
+        y, _ = oracle.fused_conv(t["x"], t["w"], t["b"], t["z"], **case.attrs())
+        dt = time.perf_counter() - t0
+        if k >= args.warmup:
+            secs += dt
+            flops += 2.0 * y.size * np.prod(case.w_shape[1:])
+    value = flops / secs / 1e12
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+           "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(secs * 1e3 / args.steps, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded, same generator as the GPU arm)",
+           "config": {"workload": "fusedconv_suite: 11 convs of the 5 benchmark workloads; "
+                                  "each step one conv, batch-1 sample, round robin"},
+           "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s",
+                            "cores": oracle.max_threads(), "kind": "oracle",
+                            "sample": "batch-1 sample of one suite conv per step"},
+           "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

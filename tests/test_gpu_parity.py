@@ -1,0 +1,211 @@
+"""GPU parity: the CUDA kernels (through the C ABI) against the CPU oracle, element by
+element, on identical seeded inputs.
+
+* small cases that span several tiles and ragged tails, for every route, tile width,
+  split-K factor, rank, stride/dilation/padding mode, group and activation;
+* the benchmark convolutions at full size, in the launch configuration the benchmark
+  times, compared on the first and last image of the batch (every output of those
+  images);
+* Y guard bands and NaN pre-fill catch out-of-bounds and missing writes.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from activation_implicit_gemm_gb300 import FusedConvPlan, _build, _lib
+from parity import check
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 64
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    _build.build()
+    _lib.load()
+    yield
+    lib = _lib.load()
+    assert lib.fconv_check_device(None) == 0, "a kernel reported a bounded-wait timeout"
+
+
+def to_dev(a):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def gpu_run(plan: FusedConvPlan, xd, wd, bd, zd, dtype) -> np.ndarray:
+    tdt = torch.float16 if dtype == "f16" else torch.float32
+    ny = int(np.prod(plan.y_shape))
+    buf = torch.full((ny + 2 * GUARD,), float("nan"), dtype=tdt, device="cuda")
+    buf[:GUARD] = 7.0
+    buf[-GUARD:] = 7.0
+    y = buf[GUARD:GUARD + ny].view(plan.y_shape)
+    ws = None
+    if plan.workspace_bytes:
+        ws = torch.full((plan.workspace_bytes // 4,), float("nan"), dtype=torch.float32,
+                        device="cuda")
+    plan.run(xd, wd, bd, zd, y=y, workspace=ws)
+    torch.cuda.synchronize()
+    head = buf[:GUARD].float().cpu().numpy()
+    tail = buf[-GUARD:].float().cpu().numpy()
+    assert np.all(head == 7.0) and np.all(tail == 7.0), "write outside Y"
+    return y.double().cpu().numpy()
+
+
+def compare(dtype, x, w, b, z, attrs, route="auto", split_k=0, tile_n=0, what=""):
+    dt = _lib.F16 if dtype == "f16" else _lib.F32
+    plan = FusedConvPlan(dt, x.shape, w.shape, has_bias=b is not None, has_z=z is not None,
+                         route=route, split_k=split_k, tile_n=tile_n, **attrs)
+    y = gpu_run(plan, to_dev(x), to_dev(w), to_dev(b), to_dev(z), dtype)
+    ref, absacc = oracle.fused_conv(x, w, b, z, **attrs)
+    pre = None
+    if attrs.get("activation") == "ThresholdedRelu":
+        pre, _ = oracle.fused_conv(x, w, b, z, **{**attrs, "activation": None,
+                                                  "activation_params": None})
+    alpha = (attrs.get("activation_params") or [1.0])[0]
+    kg = int(np.prod(w.shape[1:]))
+    check(y, ref, absacc, dtype, kg, activation=attrs.get("activation"), alpha=alpha,
+          pre_act=pre, what=f"{what} route={plan.route} tile={plan.tile_n} split={plan.split_k}")
+    return plan
+
+
+def inputs(seed, dtype, x_shape, w_shape, bias, zres, attrs, wscale=None):
+    ys = oracle.output_shape(x_shape, w_shape, **attrs)
+    kg = int(np.prod(w_shape[1:]))
+    x = workloads.draw(seed, x_shape, "normal", 1.0, dtype)
+    w = workloads.draw(seed + 1, w_shape, "normal", wscale or 1.0 / math.sqrt(kg), dtype)
+    b = workloads.draw(seed + 2, (w_shape[0],), "normal", 1.0, dtype) if bias else None
+    z = workloads.draw(seed + 3, ys, "normal", 1.0, dtype) if zres else None
+    return x, w, b, z
+
+
+# ----------------------------------------------------------------------------- tcgen05 path
+
+@pytest.mark.parametrize("tile_n", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("split_k", [1, 2, 3])
+def test_tc_tiles_and_splits(tile_n, split_k):
+    # 2*11*13 = 286 pixels: 3 row tiles with a ragged tail; Mg = 40; Kg = 216: 4 chunks,
+    # the last one partial
+    attrs = dict(pads=[1, 1, 1, 1], activation="LeakyRelu", activation_params=[0.1])
+    x, w, b, z = inputs(11, "f16", (2, 24, 11, 13), (40, 24, 3, 3), True, True, attrs)
+    compare("f16", x, w, b, z, attrs, route="igemm_tc", tile_n=tile_n, split_k=split_k,
+            what="tiles")
+
+
+TC_CASES = [
+    # (x_shape, w_shape, attrs, bias, z)
+    ((3, 5, 17, 9), (7, 5, 3, 3), dict(pads=[1, 0, 2, 1]), True, False),          # Kg=45: scalar B
+    ((2, 16, 300), (32, 16, 5), dict(dilations=[2], auto_pad="SAME_UPPER"), True, True),
+    ((1, 8, 257), (24, 8, 3), dict(strides=[2], auto_pad="SAME_LOWER"), False, True),
+    ((2, 12, 9, 10, 11), (16, 12, 3, 3, 3), dict(strides=[2, 2, 2], auto_pad="SAME_LOWER"),
+     True, True),
+    ((2, 12, 6, 7, 8), (24, 4, 3, 2, 3), dict(group=3, pads=[1, 0, 1, 1, 1, 0]), True, True),
+    ((2, 6, 14, 15), (9, 2, 3, 3), dict(group=3, strides=[2, 1], dilations=[1, 2],
+                                        pads=[1, 2, 0, 2]), True, False),
+    ((1, 32, 8, 8), (32, 32, 1, 1), dict(), False, False),                       # README shape
+    ((2, 3, 3, 3), (5, 3, 5, 5), dict(pads=[2, 2, 2, 2]), True, True),           # kernel > input
+    ((1, 4, 5, 5), (3, 4, 5, 5), dict(), True, False),                           # 1x1 output
+    ((4, 64, 7, 7), (200, 64, 3, 3), dict(pads=[1, 1, 1, 1], activation="Relu"), False, True),
+    ((2, 3, 30, 30), (16, 3, 7, 7), dict(strides=[4, 4], pads=[3, 3, 3, 3],
+                                         activation="Gelu"), True, False),
+    ((2, 16, 12, 12), (32, 16, 2, 2), dict(strides=[2, 2]), False, False),
+    ((2, 4, 9, 9), (4, 2, 3, 3), dict(group=2, auto_pad="VALID"), True, True),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(TC_CASES)))
+def test_tc_geometries(idx):
+    xs, ws, attrs, bias, zres = TC_CASES[idx]
+    x, w, b, z = inputs(100 + 10 * idx, "f16", xs, ws, bias, zres, attrs)
+    compare("f16", x, w, b, z, attrs, route="igemm_tc", what=f"tc case {idx}")
+    compare("f16", x, w, b, z, attrs, route="direct", what=f"direct case {idx}")
+
+
+ACTS = [(None, None), ("Relu", None), ("LeakyRelu", [0.01]), ("Sigmoid", None),
+        ("Tanh", None), ("HardSigmoid", [0.2, 0.5]), ("HardSwish", None), ("Clip", [-0.5, 0.75]),
+        ("QuickGelu", None), ("QuickGelu", [1.0]), ("Elu", [0.7]), ("Gelu", None), ("Gelu", [1.0]),
+        ("FastGelu", None), ("Softplus", None), ("ThresholdedRelu", [0.3]), ("Erf", None)]
+
+
+@pytest.mark.parametrize("act,params", ACTS)
+@pytest.mark.parametrize("route", ["igemm_tc", "direct", "depthwise"])
+def test_activations(act, params, route):
+    if route == "depthwise":
+        xs, ws, extra = (2, 8, 13, 14), (8, 1, 3, 3), dict(group=8)
+    else:
+        xs, ws, extra = (2, 16, 9, 10), (24, 16, 3, 3), dict()
+    attrs = dict(pads=[1, 1, 1, 1], activation=act, activation_params=params, **extra)
+    x, w, b, z = inputs(500, "f16", xs, ws, True, True, attrs, wscale=0.8 / math.sqrt(9))
+    compare("f16", x, w, b, z, attrs, route=route, what=f"act {act}")
+
+
+# ----------------------------------------------------------------------------- depthwise
+
+DW_CASES = [
+    ((2, 16, 20, 21), 3, dict(pads=[1, 1, 1, 1])),
+    ((1, 8, 15, 16), 5, dict(auto_pad="SAME_UPPER")),
+    ((2, 4, 30, 29), 7, dict(pads=[3, 3, 3, 3])),
+    ((2, 8, 17, 17), 3, dict(strides=[2, 2], pads=[1, 1, 1, 1])),
+    ((1, 8, 16, 19), 3, dict(dilations=[2, 3], pads=[2, 0, 1, 3])),
+    ((1, 4, 9, 9), 4, dict(pads=[1, 2, 2, 1])),
+    ((2, 3, 200, 220), 3, dict(pads=[1, 1, 1, 1])),  # several row bands per plane
+]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "f32"])
+@pytest.mark.parametrize("idx", range(len(DW_CASES)))
+def test_depthwise(idx, dtype):
+    xs, k, attrs = DW_CASES[idx]
+    C = xs[1]
+    attrs = dict(attrs, group=C, activation="Clip", activation_params=[-1.0, 1.5])
+    x, w, b, z = inputs(700 + idx, dtype, xs, (C, 1, k, k), True, True, attrs)
+    compare(dtype, x, w, b, z, attrs, route="depthwise", what=f"dw {idx}")
+
+
+# ----------------------------------------------------------------------------- direct fp32
+
+@pytest.mark.parametrize("sr", [1, 2, 3])
+def test_direct_f32_random(sr):
+    rng = np.random.default_rng(40 + sr)
+    for it in range(4):
+        G = int(rng.choice([1, 2]))
+        Cg, Mg = int(rng.integers(1, 5)), int(rng.integers(1, 6))
+        ins = [int(rng.integers(4, 12)) for _ in range(sr)]
+        ks = [int(rng.integers(1, 4)) for _ in range(sr)]
+        attrs = dict(group=G, strides=[int(rng.integers(1, 3)) for _ in range(sr)],
+                     dilations=[int(rng.integers(1, 3)) for _ in range(sr)],
+                     auto_pad="SAME_UPPER" if it % 2 else "SAME_LOWER", activation="Elu")
+        x, w, b, z = inputs(900 + 10 * it + sr, "f32", (2, G * Cg) + tuple(ins),
+                            (G * Mg, Cg) + tuple(ks), it % 2 == 0, it % 3 == 0, attrs)
+        compare("f32", x, w, b, z, attrs, route="direct", what=f"direct f32 {sr}/{it}")
+
+
+# ----------------------------------------------------------------------------- full-size configs
+
+@pytest.mark.parametrize("name", [c.name for c in workloads.ALL_CASES])
+def test_config_full_size(name):
+    """Auto-planned run at full size; every output of the first and last image checked."""
+    c = workloads.case_by_name(name)
+    attrs = c.attrs()
+    ys = oracle.output_shape(c.x_shape, c.w_shape, **attrs)
+    t = workloads.make_inputs(c, ys)
+    dt = _lib.F16 if c.dtype == "f16" else _lib.F32
+    plan = FusedConvPlan(dt, c.x_shape, c.w_shape, has_bias=c.has_bias, has_z=c.has_z, **attrs)
+    y = gpu_run(plan, to_dev(t["x"]), to_dev(t["w"]), to_dev(t["b"]), to_dev(t["z"]), c.dtype)
+    N = c.x_shape[0]
+    sample = sorted({0, N - 1})
+    xs = t["x"][sample]
+    zs = None if t["z"] is None else t["z"][sample]
+    ref, absacc = oracle.fused_conv(xs, t["w"], t["b"], zs, **attrs)
+    pre = None
+    kg = int(np.prod(c.w_shape[1:]))
+    alpha = (attrs.get("activation_params") or [1.0])[0]
+    check(y[sample], ref, absacc, c.dtype, kg, activation=attrs.get("activation"), alpha=alpha,
+          pre_act=pre, what=f"{name} route={plan.route} split={plan.split_k}")
+    assert np.isfinite(y).all()
