@@ -130,7 +130,8 @@ class FusedConvPlan:
         self.run_ptrs(x.data_ptr(), w.data_ptr(), 0 if b is None else b.data_ptr(),
                       0 if z is None else z.data_ptr(), y.data_ptr(),
                       0 if workspace is None else workspace.data_ptr(),
-                      0 if workspace is None else workspace.numel(), stream.cuda_stream)
+                      0 if workspace is None else workspace.numel() * workspace.element_size(),
+                      stream.cuda_stream)
         return y
 
     def __del__(self):
