@@ -182,6 +182,28 @@ fconv_status fconv_run(const fconv_plan* plan, const void* x, const void* w, con
  * a bounded wait gives up. FCONV_OK, FCONV_E_DEVICE_TIMEOUT or FCONV_E_CUDA. */
 fconv_status fconv_check_device(void* stream);
 
+/* fconv_run for callers that cannot allocate device memory: code running where
+ * cudaMalloc is unavailable or forbidden (inside a capture or allocator hook that must
+ * not allocate, a host callback, a plugin whose host application owns every device
+ * allocation, or a real-time path with a no-allocation rule). It takes the same
+ * arguments as fconv_run minus the workspace: the scratch that a split-K plan needs
+ * (fconv_plan_workspace_size) comes from a fixed array of FCONV_NOALLOC_SCRATCH_BYTES
+ * compiled into the library, which every GPU that loads the library keeps until the
+ * process exits. The pages this library follows have no counterpart of this call.
+ *  - A plan needing more scratch than FCONV_NOALLOC_SCRATCH_BYTES is rejected with
+ *    FCONV_E_WORKSPACE before anything is launched.
+ *  - The device is the current CUDA device; x, w, b, z, y and `stream` must belong to it.
+ *    The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - Calls share the one array per device. It keeps the last call's contents; the
+ *    kernels overwrite every scratch element they later read, so nothing is cleared.
+ *    Calls whose kernels overlap on the GPU (other streams, other host threads) race on
+ *    it: serialise them. Nothing here calls cudaMalloc, cudaFree or an allocating
+ *    library routine. */
+#define FCONV_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+fconv_status fconv_run_noalloc(const fconv_plan* plan, const void* x, const void* w,
+                               const void* b, const void* z, void* y, void* stream);
+
 void fconv_destroy(fconv_plan* plan);
 
 const char* fconv_status_string(fconv_status status);
