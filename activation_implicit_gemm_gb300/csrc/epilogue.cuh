@@ -40,6 +40,69 @@ __device__ __forceinline__ float apply_act(int act, float v, float alpha, float 
   }
 }
 
+
+// act(v) with the activation fixed at compile time. FAST selects __expf-based
+// exponentials (relative error ~1e-7, far below an f16 rounding) for f16 outputs;
+// f32 outputs use the accurate library functions. Dispatching once per group of
+// outputs (FCONV_ACT_SWITCH) keeps one activation's code in the instruction stream
+// instead of all fifteen.
+template <int ACT, bool FAST>
+__device__ __forceinline__ float act_eval(float v, float alpha, float beta) {
+  if constexpr (ACT == FCONV_ACT_NONE) {
+    return v;
+  } else if constexpr (ACT == FCONV_ACT_RELU) {
+    return fmaxf(v, 0.0f);
+  } else if constexpr (ACT == FCONV_ACT_LEAKYRELU) {
+    return v < 0.0f ? alpha * v : v;
+  } else if constexpr (ACT == FCONV_ACT_SIGMOID) {
+    return FAST ? __fdividef(1.0f, 1.0f + __expf(-v)) : 1.0f / (1.0f + expf(-v));
+  } else if constexpr (ACT == FCONV_ACT_TANH) {
+    return tanhf(v);
+  } else if constexpr (ACT == FCONV_ACT_HARDSIGMOID) {
+    return fminf(fmaxf(alpha * v + beta, 0.0f), 1.0f);
+  } else if constexpr (ACT == FCONV_ACT_HARDSWISH) {
+    return v * fminf(fmaxf(v * (1.0f / 6.0f) + 0.5f, 0.0f), 1.0f);
+  } else if constexpr (ACT == FCONV_ACT_CLIP) {
+    return fminf(fmaxf(v, alpha), beta);
+  } else if constexpr (ACT == FCONV_ACT_QUICKGELU) {
+    return FAST ? __fdividef(v, 1.0f + __expf(-alpha * v)) : v / (1.0f + expf(-alpha * v));
+  } else if constexpr (ACT == FCONV_ACT_ELU) {
+    return v > 0.0f ? v : alpha * (FAST ? (__expf(v) - 1.0f) : expm1f(v));
+  } else if constexpr (ACT == FCONV_ACT_GELU) {
+    if (alpha != 0.0f) return gelu_tanh_f(v);
+    return 0.5f * v * (1.0f + erff(v * 0.7071067811865476f));
+  } else if constexpr (ACT == FCONV_ACT_FASTGELU) {
+    return gelu_tanh_f(v);
+  } else if constexpr (ACT == FCONV_ACT_SOFTPLUS) {
+    return FAST ? fmaxf(v, 0.0f) + __logf(1.0f + __expf(-fabsf(v)))
+                : fmaxf(v, 0.0f) + log1pf(expf(-fabsf(v)));
+  } else if constexpr (ACT == FCONV_ACT_THRESHOLDEDRELU) {
+    return v > alpha ? v : 0.0f;
+  } else {
+    return erff(v);
+  }
+}
+
+// Calls BODY(ACT) with ACT a compile-time activation id equal to the runtime `act`.
+#define FCONV_ACT_SWITCH(act, BODY)                        \
+  switch (act) {                                           \
+    case FCONV_ACT_RELU: BODY(FCONV_ACT_RELU); break;      \
+    case FCONV_ACT_LEAKYRELU: BODY(FCONV_ACT_LEAKYRELU); break; \
+    case FCONV_ACT_SIGMOID: BODY(FCONV_ACT_SIGMOID); break; \
+    case FCONV_ACT_TANH: BODY(FCONV_ACT_TANH); break;      \
+    case FCONV_ACT_HARDSIGMOID: BODY(FCONV_ACT_HARDSIGMOID); break; \
+    case FCONV_ACT_HARDSWISH: BODY(FCONV_ACT_HARDSWISH); break; \
+    case FCONV_ACT_CLIP: BODY(FCONV_ACT_CLIP); break;      \
+    case FCONV_ACT_QUICKGELU: BODY(FCONV_ACT_QUICKGELU); break; \
+    case FCONV_ACT_ELU: BODY(FCONV_ACT_ELU); break;        \
+    case FCONV_ACT_GELU: BODY(FCONV_ACT_GELU); break;      \
+    case FCONV_ACT_FASTGELU: BODY(FCONV_ACT_FASTGELU); break; \
+    case FCONV_ACT_SOFTPLUS: BODY(FCONV_ACT_SOFTPLUS); break; \
+    case FCONV_ACT_THRESHOLDEDRELU: BODY(FCONV_ACT_THRESHOLDEDRELU); break; \
+    case FCONV_ACT_ERF: BODY(FCONV_ACT_ERF); break;        \
+    default: BODY(FCONV_ACT_NONE); break;                  \
+  }
+
 template <typename T> __device__ __forceinline__ float to_f32(T v);
 template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
 template <> __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }

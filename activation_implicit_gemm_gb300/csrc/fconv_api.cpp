@@ -184,17 +184,12 @@ void plan_igemm(fconv_plan* p, const fconv_options* o) {
   int split = 1;
   if (o && o->split_k > 0) {
     split = o->split_k;
-  } else {
-    const size_t smem = igemm_tc_smem_bytes(c.tile_n, c.stages);
-    long long per_sm = (long long)(220 * 1024) / (long long)(smem + 1024);
-    if (per_sm < 1) per_sm = 1;
-    const long long slots = (long long)p->sms * per_sm;
-    if (tiles < slots && chunks >= 2) {
-      long long s = slots / tiles;
-      if (s > chunks) s = chunks;
-      if (s > 16) s = 16;
-      split = (int)(s < 1 ? 1 : s);
-    }
+  } else if (tiles * 2 <= p->sms && chunks >= 2) {
+    // one persistent CTA per SM: split K only when at least two splits fit per tile
+    long long s = p->sms / tiles;
+    if (s > chunks) s = chunks;
+    if (s > 16) s = 16;
+    split = (int)(s < 1 ? 1 : s);
   }
   if (split > chunks) split = chunks;
   if (split < 1) split = 1;
@@ -202,6 +197,8 @@ void plan_igemm(fconv_plan* p, const fconv_options* o) {
   const int per = (chunks + split - 1) / split;
   split = (chunks + per - 1) / per;
   c.split_k = split;
+  const long long units = tiles * split;
+  c.grid = units < p->sms ? units : p->sms;
   p->workspace = igemm_tc_workspace_bytes(g, c);
 }
 

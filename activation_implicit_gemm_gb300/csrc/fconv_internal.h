@@ -42,7 +42,8 @@ struct ConvArgs {
 struct IgemmConfig {
   int tile_n;      // MMA N (channels per tile): 16..256, multiple of 16
   int split_k;     // number of K splits (>= 1)
-  int stages;      // shared-memory pipeline depth
+  int stages;      // shared-memory pipeline depth (even)
+  long long grid;  // persistent CTAs (one per SM at most)
 };
 
 // Launchers: return cudaError_t as int (0 = success).

@@ -57,6 +57,21 @@ __device__ __forceinline__ void stage_input(const ConvGeom& g, const T* __restri
   }
 }
 
+// + Z, activation and rounding of one run of up to VW outputs (activation fixed at
+// compile time; f16 outputs use the fast exponentials).
+template <int ACT, typename T, int VW>
+__device__ __forceinline__ void store_run(const float (&acc)[VW], const T* __restrict__ z,
+                                          T* __restrict__ y, long long o, int nv, float alpha,
+                                          float beta) {
+  float zv[VW];
+#pragma unroll
+  for (int j = 0; j < VW; ++j) zv[j] = (z && j < nv) ? to_f32(z[o + j]) : 0.0f;
+#pragma unroll
+  for (int j = 0; j < VW; ++j)
+    if (j < nv)
+      y[o + j] = from_f32<T>(act_eval<ACT, sizeof(T) == 2>(acc[j] + zv[j], alpha, beta));
+}
+
 // Fast path: stride 1 and dilation 1 along W, KW known at compile time.
 template <typename T, int KW, int VW>
 __global__ void __launch_bounds__(kDwThreads) dw_kernel_fast(ConvGeom g, const T* __restrict__ x,
@@ -104,14 +119,10 @@ __global__ void __launch_bounds__(kDwThreads) dw_kernel_fast(ConvGeom g, const T
       }
     }
     const long long o = ybase + (long long)oh * g.OW + ow0;
-#pragma unroll
-    for (int j = 0; j < VW; ++j) {
-      if (ow0 + j < g.OW) {
-        float v = acc[j];
-        if (z) v += to_f32(z[o + j]);
-        y[o + j] = from_f32<T>(apply_act(g.act, v, g.alpha, g.beta));
-      }
-    }
+    const int nv = min(VW, g.OW - ow0);
+#define FCONV_DW_STORE(ACT) store_run<ACT, T, VW>(acc, z, y, o, nv, g.alpha, g.beta)
+    FCONV_ACT_SWITCH(g.act, FCONV_DW_STORE)
+#undef FCONV_DW_STORE
   }
 }
 

@@ -1,40 +1,51 @@
 // Implicit-GEMM FusedConv on the 5th-generation tensor cores (tcgen05, sm_103a).
 //
 // GEMM view per group g (the package's implicit im2col routes, README variants
-// implicit_im2col_tiled_reg / implicit_im2col_subgroup_matrix: "gathers logical im2col
-// elements directly from X ... avoiding a materialized column scratch buffer"):
+// implicit_im2col_tiled_reg / implicit_im2col_subgroup_matrix: im2col elements are
+// gathered straight from X into the GEMM tiles, "avoiding a materialized column scratch
+// buffer"):
 //   rows    = output pixels q = (n, od, oh, ow)            MMA M = 128 per tile
-//   columns = output channels of the group (Mg)            MMA N = tile_n (16..256)
-//   depth   = k = (ci, kz, ky, kx), Kg = C/group * prod(k) consumed 64 at a time
+//   columns = output channels of the group (Mg)            MMA N = BN (16..256)
+//   depth   = k over (ci, tap), Kg = C/group * prod(kernel), consumed 64 per chunk
 //   A[q, k] = X[n, g*Cg + ci, od*sD - pD + kz*dD, oh*sH - pH + ky*dH, ow*sW - pW + kx*dW]
-//             (0 outside X),  B[m, k] = W[g*Mg + m, ci, kz, ky, kx]
+//             (0 outside X),   B[m, k] = W[g*Mg + m, ci, kz, ky, kx]
+// The K order is a free choice as long as A and B agree. With C/group a multiple of 8
+// the kernel uses k = tap*Cg + ci ("channel-inner"): every 8-wide piece of a row is 8
+// channels of one tap, so its validity is one test and its addresses one stride apart.
+// The weights are then read from a copy in that order (prep_weights_kernel, into the
+// workspace); otherwise k = ci*KV + tap, W's own order.
 //
-// One CTA computes a 128 x tile_n output tile over a range of K chunks:
-//   warps 0-3  gather A: thread t owns tile row t (one output pixel) and writes its 64
-//              k values of the chunk as eight 16-byte pieces into the 128B-swizzled,
-//              K-major shared-memory layout the MMA descriptor reads;
-//   warp 5     loads B (weights, already K-major in OIDHW memory) the same way;
-//   warp 4     allocates the TMEM accumulator (128 lanes x tile_n f32 columns), and one
-//              lane issues tcgen05.mma (K = 16 per instruction) and tcgen05.commit;
-//   warps 0-3  after the last chunk read the accumulator with tcgen05.ld (lane = pixel,
-//              column = channel) and run the fused epilogue: + B[m] + Z, activation,
-//              one rounding to f16, store to NCDHW Y.
-// A shared-memory ring of `stages` chunks with full/empty mbarriers overlaps gather,
-// weight loads and MMAs.
+// Persistent, warp-specialised CTA (one per SM), 14 warps:
+//   warps 0-3   epilogue: tcgen05.ld of an accumulator (lane = pixel, column = channel),
+//               + B[m] + Z, activation, one rounding to f16, NC(D)HW store;
+//   warps 4-11  A gather, two sets of four warps taking alternate K chunks; thread t of a
+//               set owns tile row t (one output pixel), loads its 64 k values of the chunk
+//               (64 loads in flight) and writes them as eight 16-byte pieces into the
+//               128-byte-swizzled K-major layout the MMA descriptor reads;
+//   warp 12     allocates TMEM (two accumulators of BN f32 columns, so the epilogue of
+//               one tile overlaps the main loop of the next) and one lane issues
+//               tcgen05.mma (K = 16 each) and tcgen05.commit;
+//   warp 13     one lane streams the weight tiles with TMA (zero fill past the edges).
+// A ring of `stages` shared-memory chunks (A 16 KB + B BN*128 B each) with full/empty
+// mbarriers connects gather/TMA -> MMA; acc_full/acc_empty connect MMA <-> epilogue.
 //
-// Split-K (the package's implicit_im2col_tiled_reg_splitk variants: "partitions the ...
-// reduction across workgroups when the unsplit output grid is too small, then combines
-// raw partial sums and applies the bias and fused activation once"): with split_k > 1
-// each CTA writes raw f32 partial sums to the workspace and splitk_reduce_kernel adds
-// the splits in a fixed order (deterministic), then applies B, Z and the activation.
+// Split-K (README variants implicit_im2col_tiled_reg_splitk: the reduction is
+// partitioned when the unsplit grid is too small, raw partial sums are combined, and
+// the bias and activation are applied once): a work unit is (tile, split); units of a
+// split plan write raw f32 partials to the workspace and splitk_reduce_kernel adds the
+// splits in a fixed order, then applies B, Z and the activation (deterministic).
 //
-// Every mbarrier wait is bounded in time; a wait that gives up sets a shared abort flag
-// and the device error word, and the CTA drains its MMAs, frees TMEM and exits.
+// Every mbarrier wait is bounded in time (2 s); a wait that gives up sets a shared abort
+// flag and the device error word, and the CTA stops issuing work, drains its MMAs,
+// frees TMEM and exits.
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <climits>
 #include <cstdint>
+#include <cstring>
+#include <mutex>
 
 #include "epilogue.cuh"
 #include "fconv_internal.h"
@@ -48,28 +59,38 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kThreads = 192;
+constexpr int kWarps = 14;
+constexpr int kThreads = kWarps * 32;
+constexpr int kEpiWarp0 = 0;     // warps 0-3
+constexpr int kGatherWarp0 = 4;  // warps 4-11
+constexpr int kMmaWarp = 12;
+constexpr int kTmaWarp = 13;
 constexpr int kMaxStages = 8;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr int kMaxTab = 2048;    // tap (channel-inner) or k (generic) table entries
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr unsigned kErrWaitTimeout = 1u;
 
 struct TcArgs {
   const uint16_t* x;
-  const uint16_t* w;
   const __half* b;
   const __half* z;
   __half* y;
-  float* ws;           // split-K partials [split][N][M][P] (f32), or null
+  float* part;          // split-K partials [split][N][M][P] (f32), or null
   int stages;
-  int chunks;          // ceil(Kg / 64)
+  int chunks;           // ceil(Kg / 64)
   int chunks_per_split;
-  int ntiles;          // channel tiles per group
+  int split;
+  int ntiles;           // channel tiles per group
+  long long row_tiles;  // ceil(N*P / 128)
+  long long units;      // row_tiles * G * ntiles * split
 };
 
 struct SharedCtl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t acc;
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -80,7 +101,7 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((i & 127u) == 0) {
+    if ((i & 63u) == 0) {
       if (*abort_flag) return false;
       if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
         *abort_flag = 1;
@@ -91,302 +112,497 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
   }
 }
 
-template <int BN>
-__global__ void __launch_bounds__(kThreads, 1) igemm_tc_kernel(const ConvGeom g, const TcArgs a) {
-  constexpr uint32_t kTmemCols = BN < 32 ? 32 : BN;
-  constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB
+struct Unit {
+  long long rt;   // row tile
+  int grp, ct, sp;
+  int c_begin, nk;
+};
+
+__device__ __forceinline__ Unit decode_unit(long long u, const TcArgs& a, int G) {
+  Unit t;
+  t.sp = (int)(u % a.split);
+  long long r = u / a.split;
+  const int gct = (int)(r % ((long long)G * a.ntiles));
+  t.rt = r / ((long long)G * a.ntiles);
+  t.grp = gct / a.ntiles;
+  t.ct = gct - t.grp * a.ntiles;
+  t.c_begin = t.sp * a.chunks_per_split;
+  t.nk = min(a.chunks_per_split, a.chunks - t.c_begin);
+  return t;
+}
+
+// Bias, residual, activation and f16 rounding for the (up to) 16 channels of one pixel.
+template <int ACT>
+__device__ __forceinline__ void epi_store16(const float (&v)[16], const uint32_t (&zr)[16],
+                                            const uint32_t (&br)[16], bool hz, bool hb,
+                                            int nvalid, __half* yp, long long P, float alpha,
+                                            float beta) {
+#pragma unroll
+  for (int jj = 0; jj < 16; ++jj) {
+    if (jj < nvalid) {
+      float t = v[jj];
+      if (hb) t += __half2float(__ushort_as_half((unsigned short)br[jj]));
+      if (hz) t += __half2float(__ushort_as_half((unsigned short)zr[jj]));
+      yp[(long long)jj * P] = __float2half_rn(act_eval<ACT, true>(t, alpha, beta));
+    }
+  }
+}
+
+template <int BN, bool CHAN>
+__global__ void __launch_bounds__(kThreads, 1)
+    igemm_tc_kernel(const ConvGeom g, const TcArgs a, const __grid_constant__ CUtensorMap tmap_w) {
+  constexpr uint32_t kAccCols = BN < 32 ? 32 : BN;
+  constexpr uint32_t kTmemCols = 2 * kAccCols;  // 64..512, a power of two
+  constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB
   constexpr uint32_t kBBytes = BN * kBK * 2;
+  constexpr uint32_t kStageBytes = kABytes + kBBytes;
   constexpr uint32_t kIdesc = ptx::idesc_f16_f32(kBM, BN);
 
   extern __shared__ uint8_t dsmem[];
   __shared__ SharedCtl ctl;
+  // channel-inner: per tap {offset in the X plane, kz | ky << 8 | kx << 16};
+  // generic: per k {offset from the group's first channel plane, same tap bits}
+  __shared__ int2 tab[kMaxTab];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const uint32_t raw = ptx::smem_addr(dsmem);
-  const uint32_t base = (raw + 1023u) & ~1023u;  // 1024-byte aligned operand ring
-  const uint32_t stage_bytes = kABytes + kBBytes;
-
-  const int grp = blockIdx.y / a.ntiles;
-  const int ct = blockIdx.y - grp * a.ntiles;
-  const int split = blockIdx.z;
-  const int c_begin = split * a.chunks_per_split;
-  const int c_end = min(c_begin + a.chunks_per_split, a.chunks);
-  const int nchunks = c_end - c_begin;
+  const uint32_t base = (ptx::smem_addr(dsmem) + 1023u) & ~1023u;
   const int S = a.stages;
+  const long long NP = (long long)g.N * g.P;
+  const int HW = g.IH * g.IW;
 
+  const int ntab = CHAN ? g.KV : g.Kg;
+  for (int t = tid; t < ntab && t < kMaxTab; t += kThreads) {
+    const int ci = CHAN ? 0 : t / g.KV;
+    const int tap = CHAN ? t : t - ci * g.KV;
+    const int kx = tap % g.KW, ky = (tap / g.KW) % g.KH, kz = tap / (g.KW * g.KH);
+    tab[t] = make_int2(ci * (int)g.IS + kz * g.dD * HW + ky * g.dH * g.IW + kx * g.dW,
+                       kz | (ky << 8) | (kx << 16));
+  }
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      ptx::mbar_init(ptx::smem_addr(&ctl.full[s]), 128 + 32);
+      ptx::mbar_init(ptx::smem_addr(&ctl.full[s]), 4 + 1);  // 4 gather warps + TMA
       ptx::mbar_init(ptx::smem_addr(&ctl.empty[s]), 1);
     }
-    ptx::mbar_init(ptx::smem_addr(&ctl.acc), 1);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(ptx::smem_addr(&ctl.acc_full[b]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl.acc_empty[b]), 4);  // 4 epilogue warps
+    }
+    ptx::mbar_init(ptx::smem_addr(&ctl.drain), 1);
     ctl.abort_flag = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_addr(&ctl.tmem_base), kTmemCols);
     ptx::tmem_relinquish();
   }
+  if (warp == kTmaWarp && lane == 0) ptx::prefetch_tmap(&tmap_w);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   volatile int* abort_flag = &ctl.abort_flag;
 
-  const long long NP = (long long)g.N * g.P;
-
-  if (warp < 4) {
-    // ---------------------------------------------------------------- A gather
-    const int r = tid;  // tile row
-    const long long q = (long long)blockIdx.x * kBM + r;
-    const bool row_ok = q < NP;
-    int n = 0, od = 0, oh = 0, ow = 0;
-    if (row_ok) {
-      n = (int)(q / g.P);
-      const long long o = q - (long long)n * g.P;
-      ow = (int)(o % g.OW);
-      oh = (int)((o / g.OW) % g.OH);
-      od = (int)(o / ((long long)g.OW * g.OH));
-    }
-    const int iz0 = od * g.sD - g.pD, iy0 = oh * g.sH - g.pH, ix0 = ow * g.sW - g.pW;
-    uint32_t mz = 0, my = 0, mx = 0;  // bit t: tap t along that axis lands inside X
-    for (int t = 0; t < g.KD; ++t) { const int v = iz0 + t * g.dD; if (v >= 0 && v < g.ID) mz |= 1u << t; }
-    for (int t = 0; t < g.KH; ++t) { const int v = iy0 + t * g.dH; if (v >= 0 && v < g.IH) my |= 1u << t; }
-    for (int t = 0; t < g.KW; ++t) { const int v = ix0 + t * g.dW; if (v >= 0 && v < g.IW) mx |= 1u << t; }
-    if (!row_ok) mz = 0;
-    const uint16_t* xg = a.x + ((long long)n * g.C + (long long)grp * g.Cg) * g.IS;
-    const int pix = (iz0 * g.IH + iy0) * g.IW + ix0;
-    const int HW = g.IH * g.IW;
-    const int step_y = g.dH * g.IW - g.KW * g.dW;       // toff change when kx wraps
-    const int step_z = g.dD * HW - g.KH * g.dH * g.IW;  // toff change when ky wraps
+  if (warp >= kGatherWarp0 && warp < kGatherWarp0 + 8) {
+    // ================================================================ A gather
+    const int set = (warp - kGatherWarp0) >> 2;
+    const int r = ((warp - kGatherWarp0) & 3) * 32 + lane;  // tile row
     const uint32_t swz = (uint32_t)(r & 7);
-
-    for (int i = 0; i < nchunks; ++i) {
-      const int s = i % S;
-      if (i >= S && !bounded_wait(ptx::smem_addr(&ctl.empty[s]), ((i / S) - 1) & 1, abort_flag))
-        break;
-      const int k0 = (c_begin + i) * kBK;
-      int ci = k0 / g.KV;
-      int tap = k0 - ci * g.KV;
-      int kz = tap / (g.KH * g.KW);
-      int rem = tap - kz * g.KH * g.KW;
-      int ky = rem / g.KW;
-      int kx = rem - ky * g.KW;
-      int toff = kz * g.dD * HW + ky * g.dH * g.IW + kx * g.dW;
-      const uint16_t* xc = xg + (long long)ci * g.IS + pix;
-      int k = k0;
-      const uint32_t arow = base + (uint32_t)s * stage_bytes + (uint32_t)r * 128u;
-#pragma unroll 1
-      for (int j = 0; j < 8; ++j) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          uint32_t v = 0;
-          if (k < g.Kg) {
-            if ((mz >> kz) & (my >> ky) & (mx >> kx) & 1u) v = __ldg(xc + toff);
-            ++k;
-            ++kx;
-            toff += g.dW;
-            if (kx == g.KW) {
-              kx = 0;
-              ++ky;
-              toff += step_y;
-              if (ky == g.KH) {
-                ky = 0;
-                ++kz;
-                toff += step_z;
-                if (kz == g.KD) {
-                  kz = 0;
-                  toff = 0;
-                  xc += g.IS;
-                }
-              }
-            }
-          }
-          if (e & 1) pk[e >> 1] |= v << 16;
-          else pk[e >> 1] = v;
-        }
-        ptx::st_shared_v4(arow + (((uint32_t)j ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
+    uint32_t it = 0;
+    for (long long u = blockIdx.x; u < a.units; u += gridDim.x) {
+      if (*abort_flag) break;
+      const Unit un = decode_unit(u, a, g.G);
+      const long long q = un.rt * kBM + r;
+      const bool row_ok = q < NP;
+      int n = 0, od = 0, oh = 0, ow = 0;
+      if (row_ok) {
+        n = (int)(q / g.P);
+        const long long o = q - (long long)n * g.P;
+        ow = (int)(o % g.OW);
+        oh = (int)((o / g.OW) % g.OH);
+        od = (int)(o / ((long long)g.OW * g.OH));
       }
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(ptx::smem_addr(&ctl.full[s]));
+      const int iz0 = od * g.sD - g.pD, iy0 = oh * g.sH - g.pH, ix0 = ow * g.sW - g.pW;
+      uint32_t mz = 0, my = 0, mx = 0;  // bit t: tap t along that axis lands inside X
+      for (int t = 0; t < g.KD; ++t) { const int v = iz0 + t * g.dD; if (v >= 0 && v < g.ID) mz |= 1u << t; }
+      for (int t = 0; t < g.KH; ++t) { const int v = iy0 + t * g.dH; if (v >= 0 && v < g.IH) my |= 1u << t; }
+      for (int t = 0; t < g.KW; ++t) { const int v = ix0 + t * g.dW; if (v >= 0 && v < g.IW) mx |= 1u << t; }
+      if (!row_ok) mz = 0;
+      const uint16_t* xg = a.x + ((long long)n * g.C + (long long)un.grp * g.Cg) * g.IS +
+                           ((iz0 * g.IH + iy0) * g.IW + ix0);
+      for (int i = 0; i < un.nk; ++i, ++it) {
+        if ((int)(it & 1u) != set) continue;
+        const int s = (int)(it % (uint32_t)S);
+        if (it >= (uint32_t)S &&
+            !bounded_wait(ptx::smem_addr(&ctl.empty[s]), ((it / S) - 1) & 1, abort_flag))
+          break;
+        const int k0 = (un.c_begin + i) * kBK;
+        uint32_t v[64];
+        if (CHAN) {
+          // eight pieces of 8 channels; each piece is one tap: one validity test, eight
+          // loads one channel plane apart, all 64 loads in flight before any store
+          int tap = k0 / g.Cg;
+          int ci = k0 - tap * g.Cg;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int kk = k0 + 8 * j;
+            uint32_t ok = 0;
+            const uint16_t* p = xg;
+            if (kk < g.Kg) {
+              const int2 ti = tab[tap];
+              ok = ((mz >> (ti.y & 0xff)) & (my >> ((ti.y >> 8) & 0xff)) & (mx >> (ti.y >> 16))) & 1u;
+              p = xg + (long long)ci * g.IS + ti.x;
+            }
+            ptx::ld8_u16(*reinterpret_cast<uint32_t(*)[8]>(&v[8 * j]), p, g.IS * 2, ok);
+            ci += 8;
+            if (ci == g.Cg) { ci = 0; ++tap; }
+          }
+        } else {
+          // per-k table: the 64 table reads do not depend on each other or on the loads
+#pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            uint32_t ok = 0;
+            const uint16_t* p = xg;
+            if (k0 + e < g.Kg) {
+              const int2 ti = tab[k0 + e];
+              ok = ((mz >> (ti.y & 0xff)) & (my >> ((ti.y >> 8) & 0xff)) & (mx >> (ti.y >> 16))) & 1u;
+              p = xg + ti.x;
+            }
+            v[e] = ptx::ld1_u16(p, ok);
+          }
+        }
+        const uint32_t arow = base + (uint32_t)s * kStageBytes + (uint32_t)r * 128u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ptx::st_shared_pack8(arow + (((uint32_t)j ^ swz) << 4), &v[8 * j]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl.full[s]));
+      }
     }
-
-    // ---------------------------------------------------------------- epilogue
-    if (!*abort_flag && bounded_wait(ptx::smem_addr(&ctl.acc), 0, abort_flag)) {
+  } else if (warp == kTmaWarp) {
+    // ================================================================ weights by TMA
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (long long u = blockIdx.x; u < a.units; u += gridDim.x) {
+        if (*abort_flag) break;
+        const Unit un = decode_unit(u, a, g.G);
+        const int row0 = un.grp * g.Mg + un.ct * BN;
+        bool stop = false;
+        for (int i = 0; i < un.nk; ++i, ++it) {
+          const int s = (int)(it % (uint32_t)S);
+          if (it >= (uint32_t)S &&
+              !bounded_wait(ptx::smem_addr(&ctl.empty[s]), ((it / S) - 1) & 1, abort_flag)) {
+            stop = true;
+            break;
+          }
+          const uint32_t bar = ptx::smem_addr(&ctl.full[s]);
+          ptx::mbar_arrive_expect_tx(bar, kBBytes);
+          ptx::tma_load_2d(base + (uint32_t)s * kStageBytes + kABytes, &tmap_w,
+                           (un.c_begin + i) * kBK, row0, bar);
+        }
+        if (stop) break;
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ================================================================ MMA issue
+    if (lane == 0) {
+      uint32_t it = 0, tcount = 0;
+      for (long long u = blockIdx.x; u < a.units; u += gridDim.x, ++tcount) {
+        if (*abort_flag) break;
+        const Unit un = decode_unit(u, a, g.G);
+        const uint32_t b = tcount & 1u;
+        if (tcount >= 2 &&
+            !bounded_wait(ptx::smem_addr(&ctl.acc_empty[b]), ((tcount >> 1) - 1) & 1, abort_flag))
+          break;
+        ptx::tc_fence_after();
+        const uint32_t dacc = tmem + b * kAccCols;
+        bool stop = false;
+        for (int i = 0; i < un.nk; ++i, ++it) {
+          const int s = (int)(it % (uint32_t)S);
+          if (!bounded_wait(ptx::smem_addr(&ctl.full[s]), (it / S) & 1, abort_flag)) {
+            stop = true;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t abase = base + (uint32_t)s * kStageBytes;
+          const uint32_t bbase = abase + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            ptx::mma_f16(dacc, ptx::desc_sw128(abase + kk * 32), ptx::desc_sw128(bbase + kk * 32),
+                         kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(ptx::smem_addr(&ctl.empty[s]));
+        }
+        if (stop) break;
+        ptx::mma_commit(ptx::smem_addr(&ctl.acc_full[b]));
+      }
+      // every issued MMA must be complete before TMEM is freed
+      ptx::mma_commit(ptx::smem_addr(&ctl.drain));
+      bounded_wait(ptx::smem_addr(&ctl.drain), 0, abort_flag);
+    }
+  } else {
+    // ================================================================ epilogue (warps 0-3)
+    const int r = (warp - kEpiWarp0) * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp - kEpiWarp0) * 32) << 16);
+    uint32_t tcount = 0;
+    for (long long u = blockIdx.x; u < a.units; u += gridDim.x, ++tcount) {
+      if (*abort_flag) break;
+      const Unit un = decode_unit(u, a, g.G);
+      const uint32_t b = tcount & 1u;
+      if (!bounded_wait(ptx::smem_addr(&ctl.acc_full[b]), (tcount >> 1) & 1, abort_flag)) break;
       ptx::tc_fence_after();
-      const long long obase = row_ok ? (long long)n * g.M * g.P + (q - (long long)n * g.P) : 0;
-      const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+      const long long q = un.rt * kBM + r;
+      const bool row_ok = q < NP;
+      long long obase = 0;
+      if (row_ok) {
+        const long long n = q / g.P;
+        obase = n * g.M * g.P + (q - n * g.P);
+      }
+      const int mc0 = un.ct * BN;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         float v[16];
-        ptx::tmem_ld16(lane_addr + (uint32_t)c0, v);
+        __syncwarp();
+        ptx::tmem_ld16(lane_base + b * kAccCols + (uint32_t)c0, v);
         if (!row_ok) continue;
+        const int mcb = mc0 + c0;
+        const int nvalid = min(16, g.Mg - mcb);
+        if (nvalid <= 0) continue;
+        const long long yb = obase + (long long)(un.grp * g.Mg + mcb) * g.P;
+        if (a.part) {
+          float* pp = a.part + (long long)un.sp * NP * g.M + yb;
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const int mc = ct * BN + c0 + jj;
-          if (mc >= g.Mg) break;
-          const int m = grp * g.Mg + mc;
-          const long long yi = obase + (long long)m * g.P;
-          if (a.ws) {
-            a.ws[(long long)split * NP * g.M + yi] = v[jj];
-          } else {
-            float t = v[jj];
-            if (a.b) t += __half2float(a.b[m]);
-            if (a.z) t += __half2float(a.z[yi]);
-            a.y[yi] = __float2half_rn(apply_act(g.act, t, g.alpha, g.beta));
-          }
+          for (int jj = 0; jj < 16; ++jj)
+            if (jj < nvalid) pp[(long long)jj * g.P] = v[jj];
+          continue;
         }
-      }
-    }
-  } else if (warp == 5) {
-    // ---------------------------------------------------------------- B (weights)
-    const bool vec = (g.Kg & 7) == 0;
-    for (int i = 0; i < nchunks; ++i) {
-      const int s = i % S;
-      if (i >= S && !bounded_wait(ptx::smem_addr(&ctl.empty[s]), ((i / S) - 1) & 1, abort_flag))
-        break;
-      const int k0 = (c_begin + i) * kBK;
-      const uint32_t bbase = base + (uint32_t)s * stage_bytes + kABytes;
-      for (int p = lane; p < BN * 8; p += 32) {
-        const int ml = p >> 3, j = p & 7;
-        const int mc = ct * BN + ml;
-        const int k = k0 + j * 8;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (mc < g.Mg && k < g.Kg) {
-          const uint16_t* wp = a.w + (long long)(grp * g.Mg + mc) * g.Kg + k;
-          if (vec) {
-            v = ptx::ldg_nc_v4(wp);
-          } else {
-            uint32_t e[8];
+        // all loads of the 16 outputs first (Z one channel plane apart, B broadcast),
+        // then the math and the stores
+        uint32_t zr[16], br[16];
+        if (a.z) {
 #pragma unroll
-            for (int t = 0; t < 8; ++t) e[t] = (k + t < g.Kg) ? (uint32_t)__ldg(wp + t) : 0u;
-            v = make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16),
-                           e[6] | (e[7] << 16));
-          }
+          for (int jj = 0; jj < 16; ++jj)
+            zr[jj] = ptx::ld1_u16(a.z + yb + (long long)jj * g.P, jj < nvalid ? 1u : 0u);
         }
-        ptx::st_shared_v4(bbase + (uint32_t)ml * 128u + ((uint32_t)(j ^ (ml & 7)) << 4), v.x, v.y,
-                          v.z, v.w);
-      }
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(ptx::smem_addr(&ctl.full[s]));
-    }
-  } else if (warp == 4 && lane == 0) {
-    // ---------------------------------------------------------------- MMA issue
-    for (int i = 0; i < nchunks; ++i) {
-      const int s = i % S;
-      if (!bounded_wait(ptx::smem_addr(&ctl.full[s]), (i / S) & 1, abort_flag)) break;
-      ptx::tc_fence_after();
-      const uint32_t abase = base + (uint32_t)s * stage_bytes;
-      const uint32_t bbase = abase + kABytes;
+        if (a.b) {
+          const __half* bp = a.b + un.grp * g.Mg + mcb;
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk) {
-        ptx::mma_f16(tmem, ptx::desc_sw128(abase + kk * 32), ptx::desc_sw128(bbase + kk * 32),
-                     kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int jj = 0; jj < 16; ++jj) br[jj] = ptx::ld1_u16(bp + jj, jj < nvalid ? 1u : 0u);
+        }
+        __half* yp = a.y + yb;
+        const bool hz = a.z != nullptr, hb = a.b != nullptr;
+#define FCONV_EPI16(ACT) epi_store16<ACT>(v, zr, br, hz, hb, nvalid, yp, g.P, g.alpha, g.beta)
+        FCONV_ACT_SWITCH(g.act, FCONV_EPI16)
+#undef FCONV_EPI16
       }
-      ptx::mma_commit(ptx::smem_addr(&ctl.empty[s]));
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl.acc_empty[b]));
     }
-    ptx::mma_commit(ptx::smem_addr(&ctl.acc));
-    // do not free TMEM before every issued MMA has finished
-    bounded_wait(ptx::smem_addr(&ctl.acc), 0, abort_flag);
   }
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
+    __syncwarp();
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
   }
 }
 
+// Weights in the GEMM's K order, zero padded to kpad columns: wp[m][k'] for k' < kpad.
+__global__ void __launch_bounds__(256) prep_weights_kernel(const uint16_t* __restrict__ w,
+                                                           uint16_t* __restrict__ wp, int M,
+                                                           int Cg, int KV, int kpad, int chan) {
+  const long long total = (long long)M * kpad;
+  const int Kg = Cg * KV;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int m = (int)(i / kpad);
+    const int k = (int)(i - (long long)m * kpad);
+    uint16_t v = 0;
+    if (k < Kg) {
+      int src = k;
+      if (chan) {
+        const int tap = k / Cg, ci = k - tap * Cg;
+        src = ci * KV + tap;
+      }
+      v = w[(long long)m * Kg + src];
+    }
+    wp[i] = v;
+  }
+}
+
 // Y = act(sum_s partial[s] + B + Z), the splits added in order 0..S-1.
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const ConvGeom g, const float* ws,
+template <int ACT>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const ConvGeom g, const float* part,
                                                             int splits, const __half* b,
                                                             const __half* z, __half* y,
                                                             long long total) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
-    float acc = ws[i];
-    for (int s = 1; s < splits; ++s) acc += ws[(long long)s * total + i];
+    float acc = part[i];
+    for (int s = 1; s < splits; ++s) acc += part[(long long)s * total + i];
     const int m = (int)((i / g.P) % g.M);
     if (b) acc += __half2float(b[m]);
     if (z) acc += __half2float(z[i]);
-    y[i] = __float2half_rn(apply_act(g.act, acc, g.alpha, g.beta));
+    y[i] = __float2half_rn(act_eval<ACT, true>(acc, g.alpha, g.beta));
   }
 }
 
-template <int BN>
-int launch_bn(const ConvGeom& g, const IgemmConfig& c, const TcArgs& ta, cudaStream_t s) {
+// ------------------------------------------------------------------- host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)p;
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+bool channel_inner(const ConvGeom& g) { return (g.Cg % 8) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+template <int BN, bool CHAN>
+int launch_t(const ConvGeom& g, const IgemmConfig& c, const TcArgs& ta, const CUtensorMap& tm,
+             cudaStream_t s) {
   const size_t smem = igemm_tc_smem_bytes(BN, c.stages);
-  cudaError_t e = cudaFuncSetAttribute(igemm_tc_kernel<BN>,
+  cudaError_t e = cudaFuncSetAttribute(igemm_tc_kernel<BN, CHAN>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  const long long rows = ((long long)g.N * g.P + kBM - 1) / kBM;
-  dim3 grid((unsigned)rows, (unsigned)(g.G * ta.ntiles), (unsigned)c.split_k);
-  igemm_tc_kernel<BN><<<grid, kThreads, smem, s>>>(g, ta);
+  igemm_tc_kernel<BN, CHAN><<<(unsigned)c.grid, kThreads, smem, s>>>(g, ta, tm);
   return (int)cudaGetLastError();
+}
+
+template <bool CHAN>
+int launch_bn(const ConvGeom& g, const IgemmConfig& c, const TcArgs& ta, const CUtensorMap& tm,
+              cudaStream_t s) {
+  switch (c.tile_n) {
+    case 16: return launch_t<16, CHAN>(g, c, ta, tm, s);
+    case 32: return launch_t<32, CHAN>(g, c, ta, tm, s);
+    case 64: return launch_t<64, CHAN>(g, c, ta, tm, s);
+    case 128: return launch_t<128, CHAN>(g, c, ta, tm, s);
+    case 256: return launch_t<256, CHAN>(g, c, ta, tm, s);
+    default: return (int)cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
 int igemm_tc_stages(int tile_n) {
-  if (tile_n >= 256) return 4;
-  if (tile_n >= 128) return 6;
-  return 4;
+  const int per = kBM * kBK * 2 + tile_n * kBK * 2;
+  int st = (200 * 1024) / per;
+  if (st > kMaxStages) st = kMaxStages;
+  st &= ~1;  // the two gather sets alternate chunks: an even ring
+  return st < 2 ? 2 : st;
 }
 
 size_t igemm_tc_smem_bytes(int tile_n, int stages) {
   return (size_t)stages * (size_t)(kBM * kBK * 2 + tile_n * kBK * 2) + 1024;
 }
 
+// Weight copy in GEMM order (when W itself cannot be read by TMA in that order).
+static bool needs_prep(const ConvGeom& g) {
+  if (channel_inner(g)) return !(g.KV == 1);  // 1x1: channel-inner order is W's order
+  return (g.Kg % 8) != 0;                       // TMA rows must be 16-byte multiples
+}
+
+static size_t kpad_of(const ConvGeom& g) { return round_up((size_t)g.Kg, 8); }
+
+static size_t prep_bytes(const ConvGeom& g) {
+  return needs_prep(g) ? round_up((size_t)g.M * kpad_of(g) * 2, 1024) : 0;
+}
+
 size_t igemm_tc_workspace_bytes(const ConvGeom& g, const IgemmConfig& c) {
-  if (c.split_k <= 1) return 0;
-  return (size_t)c.split_k * (size_t)g.N * (size_t)g.M * (size_t)g.P * sizeof(float);
+  size_t b = prep_bytes(g);
+  if (c.split_k > 1) b += (size_t)c.split_k * (size_t)g.N * (size_t)g.M * (size_t)g.P * 4;
+  return b;
 }
 
 bool igemm_tc_supported(const ConvGeom& g) {
   if (g.dtype != FCONV_F16) return false;
   if (g.KD > 32 || g.KH > 32 || g.KW > 32) return false;
+  if (channel_inner(g) ? g.KV > kMaxTab : g.Kg > kMaxTab) return false;
+  // generic order: the per-k table holds ci * plane offsets in 32-bit ints
+  if (!channel_inner(g) && (long long)g.Cg * g.IS > INT_MAX / 2) return false;
   // in-plane offsets, including those of padded taps, stay in 32-bit ints
   const long long span = (long long)(g.ID + g.pD + 1) * (g.IH + g.pH + 1) * (g.IW + g.pW + 1);
   if (span > INT_MAX / 2) return false;
-  const long long rows = ((long long)g.N * g.P + kBM - 1) / kBM;
-  if (rows > INT_MAX) return false;
-  if ((long long)g.G * ((g.Mg + 15) / 16) > 65535) return false;
+  if ((long long)g.M * (long long)kpad_of(g) > INT_MAX) return false;
   return true;
 }
 
 int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, void* stream) {
   cudaStream_t s = (cudaStream_t)stream;
+  if (c.stages < 2 || c.stages > kMaxStages || (c.stages & 1)) return (int)cudaErrorInvalidValue;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return (int)cudaErrorNotSupported;
+  const bool chan = channel_inner(g);
+  const uint16_t* wmat = (const uint16_t*)a.w;
+  uint8_t* ws = (uint8_t*)a.ws;
+  const size_t pb = prep_bytes(g);
+  const int kpad = (int)kpad_of(g);
+  if (pb) {
+    uint16_t* wp = (uint16_t*)ws;
+    const long long total = (long long)g.M * kpad;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 152LL * 16) blocks = 152LL * 16;
+    prep_weights_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)a.w, wp, g.M, g.Cg,
+                                                         g.KV, kpad, chan ? 1 : 0);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
+    wmat = wp;
+  }
+  const int wcols = pb ? kpad : g.Kg;
+  CUtensorMap tm;
+  std::memset(&tm, 0, sizeof(tm));
+  cuuint64_t dims[2] = {(cuuint64_t)wcols, (cuuint64_t)g.M};
+  cuuint64_t strides[1] = {(cuuint64_t)wcols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)c.tile_n};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult cr = enc(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (void*)wmat, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return (int)cudaErrorInvalidValue;
+
   TcArgs ta;
   ta.x = (const uint16_t*)a.x;
-  ta.w = (const uint16_t*)a.w;
   ta.b = (const __half*)a.b;
   ta.z = (const __half*)a.z;
   ta.y = (__half*)a.y;
-  ta.ws = c.split_k > 1 ? (float*)a.ws : nullptr;
+  ta.part = c.split_k > 1 ? (float*)(ws + pb) : nullptr;
   ta.stages = c.stages;
   ta.chunks = (g.Kg + kBK - 1) / kBK;
   ta.chunks_per_split = (ta.chunks + c.split_k - 1) / c.split_k;
+  ta.split = c.split_k;
   ta.ntiles = (g.Mg + c.tile_n - 1) / c.tile_n;
-  if (c.stages < 2 || c.stages > kMaxStages) return (int)cudaErrorInvalidValue;
-  int err;
-  switch (c.tile_n) {
-    case 16: err = launch_bn<16>(g, c, ta, s); break;
-    case 32: err = launch_bn<32>(g, c, ta, s); break;
-    case 64: err = launch_bn<64>(g, c, ta, s); break;
-    case 128: err = launch_bn<128>(g, c, ta, s); break;
-    case 256: err = launch_bn<256>(g, c, ta, s); break;
-    default: return (int)cudaErrorInvalidValue;
-  }
+  ta.row_tiles = ((long long)g.N * g.P + kBM - 1) / kBM;
+  ta.units = ta.row_tiles * g.G * ta.ntiles * c.split_k;
+  const int err = chan ? launch_bn<true>(g, c, ta, tm, s) : launch_bn<false>(g, c, ta, tm, s);
   if (err != 0 || c.split_k <= 1) return err;
   const long long total = (long long)g.N * g.M * g.P;
   long long blocks = (total + 255) / 256;
   if (blocks > 152LL * 32) blocks = 152LL * 32;
-  splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(g, (const float*)a.ws, c.split_k, ta.b,
-                                                        ta.z, ta.y, total);
+#define FCONV_REDUCE(ACT)                                                                  \
+  splitk_reduce_kernel<ACT><<<(unsigned)blocks, 256, 0, s>>>(g, ta.part, c.split_k, ta.b, ta.z, \
+                                                             ta.y, total)
+  FCONV_ACT_SWITCH(g.act, FCONV_REDUCE)
+#undef FCONV_REDUCE
   return (int)cudaGetLastError();
 }
 

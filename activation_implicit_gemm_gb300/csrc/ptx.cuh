@@ -140,5 +140,74 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   return v;
 }
 
+
+// Arrive on `bar` and add `bytes` to the transaction count the phase waits for.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar), "r"(bytes)
+      : "memory");
+}
+
+// 2-D tiled TMA load of one box into shared memory; completion is signalled on `bar`
+// as transaction bytes. c0 is the innermost (contiguous) coordinate.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int c0, int c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"((uint64_t)tmap), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)tmap) : "memory");
+}
+
+// Eight predicated 16-bit global loads at p, p + stride, ..., p + 7*stride (bytes),
+// issued back to back; each result is zero-extended into 32 bits (0 when !pred).
+__device__ __forceinline__ void ld8_u16(uint32_t (&v)[8], const void* p, long long stride,
+                                        uint32_t pred) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t.reg .b64 a;\n\t"
+      "setp.ne.b32 q, %10, 0;\n\t"
+      "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\tmov.b32 %3, 0;\n\t"
+      "mov.b32 %4, 0;\n\tmov.b32 %5, 0;\n\tmov.b32 %6, 0;\n\tmov.b32 %7, 0;\n\t"
+      "mov.b64 a, %8;\n\t"
+      "@q ld.global.nc.u16 %0, [a];\n\tadd.s64 a, a, %9;\n\t"
+      "@q ld.global.nc.u16 %1, [a];\n\tadd.s64 a, a, %9;\n\t"
+      "@q ld.global.nc.u16 %2, [a];\n\tadd.s64 a, a, %9;\n\t"
+      "@q ld.global.nc.u16 %3, [a];\n\tadd.s64 a, a, %9;\n\t"
+      "@q ld.global.nc.u16 %4, [a];\n\tadd.s64 a, a, %9;\n\t"
+      "@q ld.global.nc.u16 %5, [a];\n\tadd.s64 a, a, %9;\n\t"
+      "@q ld.global.nc.u16 %6, [a];\n\tadd.s64 a, a, %9;\n\t"
+      "@q ld.global.nc.u16 %7, [a];\n\t}"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7])
+      : "l"(p), "l"(stride), "r"(pred));
+}
+
+// One predicated 16-bit global load, zero-extended (0 when !pred).
+__device__ __forceinline__ uint32_t ld1_u16(const void* p, uint32_t pred) {
+  uint32_t v;
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\tmov.b32 %0, 0;\n\t"
+      "@q ld.global.nc.u16 %0, [%1];\n\t}"
+      : "=r"(v)
+      : "l"(p), "r"(pred));
+  return v;
+}
+
+// Pack eight zero-extended 16-bit values into 16 bytes and store them to shared memory.
+__device__ __forceinline__ void st_shared_pack8(uint32_t addr, const uint32_t* v) {
+  asm volatile(
+      "{\n\t.reg .b32 p0, p1, p2, p3;\n\t"
+      "prmt.b32 p0, %1, %2, 0x5410;\n\tprmt.b32 p1, %3, %4, 0x5410;\n\t"
+      "prmt.b32 p2, %5, %6, 0x5410;\n\tprmt.b32 p3, %7, %8, 0x5410;\n\t"
+      "st.shared.v4.b32 [%0], {p0, p1, p2, p3};\n\t}" ::"r"(addr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
+}
+
 }  // namespace ptx
 }  // namespace fconv

@@ -143,7 +143,10 @@ def run_ours(args):
     peaks, peaks_kind = load_peaks()
 
     convs = []
-    for case in workloads.ALL_CASES:
+    cases = workloads.ALL_CASES
+    if args.conv:
+        cases = [workloads.case_by_name(n) for n in args.conv.split(",")]
+    for case in cases:
         t, ys = conv_tensors(case)
         dt = _lib.F16 if case.dtype == "f16" else _lib.F32
         plan = fc.FusedConvPlan(dt, case.x_shape, case.w_shape, has_bias=case.has_bias,
@@ -303,7 +306,9 @@ def run_ours(args):
                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                    "steps": e2e_steps, "api": "FusedConvPlan.run (C ABI fconv_run)"},
            "gpu_launches": launches_per_step * K, "clocks": clocks}
-    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+    if args.conv:
+        out["config"]["workload"] = "subset: " + args.conv
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline and not args.conv:
         out["cpu_baseline"] = cpu_baseline()
     if rank == 0:
         print(json.dumps(out), flush=True)
@@ -383,6 +388,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--conv", default="",
+                    help="comma-separated conv names: time only these (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
