@@ -148,6 +148,22 @@ __device__ __forceinline__ void epi_store16(const float (&v)[16], const uint32_t
   }
 }
 
+// As epi_store16, but the 16 results go to this lane's column of the warp's staging tile
+// (channel-major, 64 bytes per channel row) for the vector store.
+template <int ACT>
+__device__ __forceinline__ void epi_stage16(const float (&v)[16], const uint32_t (&zr)[16],
+                                            const uint32_t (&br)[16], bool hz, bool hb,
+                                            uint32_t col, float alpha, float beta) {
+#pragma unroll
+  for (int jj = 0; jj < 16; ++jj) {
+    float t = v[jj];
+    if (hb) t += __half2float(__ushort_as_half((unsigned short)br[jj]));
+    if (hz) t += __half2float(__ushort_as_half((unsigned short)zr[jj]));
+    const __half h = __float2half_rn(act_eval<ACT, true>(t, alpha, beta));
+    ptx::st_shared_u16(col + jj * 64, __half_as_ushort(h));
+  }
+}
+
 template <int BN, bool CHAN>
 __global__ void __launch_bounds__(kThreads, 1)
     igemm_tc_kernel(const ConvGeom g, const TcArgs a, const __grid_constant__ CUtensorMap tmap_w) {
@@ -239,7 +255,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         const int k0 = (un.c_begin + i) * kBK;
         uint32_t v[64];
-        if (CHAN) {
+        if (CHAN && (g.Cg % kBK) == 0) {
+          // the whole chunk is 64 channels of one tap: one validity test, 64 loads one
+          // channel plane apart, all in flight before any store
+          const int tap = k0 / g.Cg;
+          const int ci = k0 - tap * g.Cg;
+          const int2 ti = tab[tap];
+          const bool ok = ((mz >> (ti.y & 0xff)) & (my >> ((ti.y >> 8) & 0xff)) & (mx >> (ti.y >> 16))) & 1u;
+          if (ok) {
+            const uint16_t* p = xg + (long long)ci * g.IS + ti.x;
+#pragma unroll
+            for (int e = 0; e < 64; ++e) v[e] = __ldg(p + (long long)e * g.IS);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) v[e] = 0u;
+          }
+        } else if (CHAN) {
           // eight pieces of 8 channels; each piece is one tap: one validity test, eight
           // loads one channel plane apart, all 64 loads in flight before any store
           int tap = k0 / g.Cg;
@@ -254,7 +285,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = ((mz >> (ti.y & 0xff)) & (my >> ((ti.y >> 8) & 0xff)) & (mx >> (ti.y >> 16))) & 1u;
               p = xg + (long long)ci * g.IS + ti.x;
             }
-            ptx::ld8_u16(*reinterpret_cast<uint32_t(*)[8]>(&v[8 * j]), p, g.IS * 2, ok);
+            uint32_t(&v8)[8] = *reinterpret_cast<uint32_t(*)[8]>(&v[8 * j]);
+            if (ok) {
+              ptx::ld8_u16_nz(v8, p, g.IS * 2);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v8[e] = 0u;
+            }
             ci += 8;
             if (ci == g.Cg) { ci = 0; ++tap; }
           }
@@ -345,6 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ epilogue (warps 0-3)
     const int r = (warp - kEpiWarp0) * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)((warp - kEpiWarp0) * 32) << 16);
+    // 16-byte Y/Z vectors need 8-pixel groups inside one image (P % 8 == 0)
+    const bool vec_io = (g.P % 8) == 0;
+    const uint32_t yst = base + (uint32_t)S * kStageBytes + (uint32_t)(warp - kEpiWarp0) * 2048u;
+    const uint32_t zst = yst + 1024u;
     uint32_t tcount = 0;
     for (long long u = blockIdx.x; u < a.units; u += gridDim.x, ++tcount) {
       if (*abort_flag) break;
@@ -360,12 +401,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         obase = n * g.M * g.P + (q - n * g.P);
       }
       const int mc0 = un.ct * BN;
+      // pixel group (8 consecutive pixels) this lane moves in the vector path
+      const long long gq = un.rt * kBM + (warp - kEpiWarp0) * 32 + (lane & 3) * 8;
+      const bool grp_ok = gq < NP;
+      const long long gn = grp_ok ? gq / g.P : 0;
+      const long long gp = grp_ok ? gq - gn * g.P : 0;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         float v[16];
         __syncwarp();
         ptx::tmem_ld16(lane_base + b * kAccCols + (uint32_t)c0, v);
-        if (!row_ok) continue;
+        // the vector path needs every lane (shuffles, warp syncs); invalid rows there are
+        // whole 8-pixel groups that are never stored
+        if (!row_ok && !(vec_io && a.part == nullptr)) continue;
         const int mcb = mc0 + c0;
         const int nvalid = min(16, g.Mg - mcb);
         if (nvalid <= 0) continue;
@@ -377,21 +425,57 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (jj < nvalid) pp[(long long)jj * g.P] = v[jj];
           continue;
         }
-        // all loads of the 16 outputs first (Z one channel plane apart, B broadcast),
-        // then the math and the stores
+        const bool hz = a.z != nullptr, hb = a.b != nullptr;
         uint32_t zr[16], br[16];
-        if (a.z) {
+        if (vec_io) {
+          // Z and Y move as 16-byte vectors (8 pixels of one channel) through this warp's
+          // staging tile [16 channels][32 pixels]; lane l owns pixel group l % 4 and
+          // channels l / 4 and l / 4 + 8 for the vector moves
+          const int m0 = un.grp * g.Mg + mcb;
+          if (hz) {
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const int ch = (lane >> 2) + 8 * t;
+              uint4 zv = make_uint4(0, 0, 0, 0);
+              if (grp_ok && ch < nvalid)
+                zv = ptx::ldg_nc_v4(a.z + ((gn * g.M + m0 + ch) * g.P + gp));
+              ptx::st_shared_v4(zst + ch * 64 + (lane & 3) * 16, zv.x, zv.y, zv.z, zv.w);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) zr[jj] = ptx::ld_shared_u16(zst + jj * 64 + lane * 2);
+          }
+          if (hb) {
+            const uint32_t bl = ptx::ld1_u16(a.b + m0 + (lane & 15), (lane & 15) < nvalid ? 1u : 0u);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) br[jj] = __shfl_sync(0xffffffffu, bl, jj);
+          }
+#define FCONV_EPI16S(ACT) epi_stage16<ACT>(v, zr, br, hz, hb, yst + lane * 2, g.alpha, g.beta)
+          FCONV_ACT_SWITCH(g.act, FCONV_EPI16S)
+#undef FCONV_EPI16S
+          __syncwarp();
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int ch = (lane >> 2) + 8 * t;
+            if (grp_ok && ch < nvalid) {
+              const uint4 yv = ptx::ld_shared_v4(yst + ch * 64 + (lane & 3) * 16);
+              ptx::st_global_v4(a.y + ((gn * g.M + m0 + ch) * g.P + gp), yv);
+            }
+          }
+          __syncwarp();
+          continue;
+        }
+        if (hz) {
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj)
             zr[jj] = ptx::ld1_u16(a.z + yb + (long long)jj * g.P, jj < nvalid ? 1u : 0u);
         }
-        if (a.b) {
+        if (hb) {
           const __half* bp = a.b + un.grp * g.Mg + mcb;
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) br[jj] = ptx::ld1_u16(bp + jj, jj < nvalid ? 1u : 0u);
         }
         __half* yp = a.y + yb;
-        const bool hz = a.z != nullptr, hb = a.b != nullptr;
 #define FCONV_EPI16(ACT) epi_store16<ACT>(v, zr, br, hz, hb, nvalid, yp, g.P, g.alpha, g.beta)
         FCONV_ACT_SWITCH(g.act, FCONV_EPI16)
 #undef FCONV_EPI16
@@ -513,7 +597,8 @@ int igemm_tc_stages(int tile_n) {
 }
 
 size_t igemm_tc_smem_bytes(int tile_n, int stages) {
-  return (size_t)stages * (size_t)(kBM * kBK * 2 + tile_n * kBK * 2) + 1024;
+  // operand ring + 1 KB alignment slack + the epilogue warps' Y/Z staging tiles
+  return (size_t)stages * (size_t)(kBM * kBK * 2 + tile_n * kBK * 2) + 1024 + 4 * 2048;
 }
 
 // Weight copy in GEMM order (when W itself cannot be read by TMA in that order).

@@ -33,14 +33,16 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
       : "memory");
 }
 
+// Test the phase with the given parity; if it is not complete the thread may be
+// suspended for up to ~20 us (the hint) or until the phase completes.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(20000)
       : "memory");
   return ok != 0;
 }
@@ -132,6 +134,28 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"((unsigned short)v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -185,6 +209,25 @@ __device__ __forceinline__ void ld8_u16(uint32_t (&v)[8], const void* p, long lo
       : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
         "=r"(v[7])
       : "l"(p), "l"(stride), "r"(pred));
+}
+
+// Eight 16-bit global loads at p + k*stride (bytes), k = 0..7, zero-extended; no
+// predicate: the caller has checked the addresses.
+__device__ __forceinline__ void ld8_u16_nz(uint32_t (&v)[8], const void* p, long long stride) {
+  const char* c = (const char*)p;
+  asm volatile(
+      "ld.global.nc.u16 %0, [%8];\n\t"
+      "ld.global.nc.u16 %1, [%9];\n\t"
+      "ld.global.nc.u16 %2, [%10];\n\t"
+      "ld.global.nc.u16 %3, [%11];\n\t"
+      "ld.global.nc.u16 %4, [%12];\n\t"
+      "ld.global.nc.u16 %5, [%13];\n\t"
+      "ld.global.nc.u16 %6, [%14];\n\t"
+      "ld.global.nc.u16 %7, [%15];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7])
+      : "l"(c), "l"(c + stride), "l"(c + 2 * stride), "l"(c + 3 * stride), "l"(c + 4 * stride),
+        "l"(c + 5 * stride), "l"(c + 6 * stride), "l"(c + 7 * stride));
 }
 
 // One predicated 16-bit global load, zero-extended (0 when !pred).

@@ -98,6 +98,17 @@ def test_tc_tiles_and_splits(tile_n, split_k):
             what="tiles")
 
 
+@pytest.mark.parametrize("tile_n", [16, 64, 256])
+@pytest.mark.parametrize("split_k", [1, 2])
+def test_tc_vector_epilogue_ragged(tile_n, split_k):
+    # P = 64 (a multiple of 8: 16-byte Y/Z path); 3*64 = 192 pixels: the second row tile
+    # is half empty; Mg = 40: the last 16-channel group has 8 valid channels
+    attrs = dict(pads=[1, 1, 1, 1], activation="QuickGelu")
+    x, w, b, z = inputs(13, "f16", (3, 16, 8, 8), (40, 16, 3, 3), True, True, attrs)
+    compare("f16", x, w, b, z, attrs, route="igemm_tc", tile_n=tile_n, split_k=split_k,
+            what="vector epilogue")
+
+
 TC_CASES = [
     # (x_shape, w_shape, attrs, bias, z)
     ((3, 5, 17, 9), (7, 5, 3, 3), dict(pads=[1, 0, 2, 1]), True, False),          # Kg=45: scalar B
@@ -139,7 +150,8 @@ def test_activations(act, params, route):
     if route == "depthwise":
         xs, ws, extra = (2, 8, 13, 14), (8, 1, 3, 3), dict(group=8)
     else:
-        xs, ws, extra = (2, 16, 9, 10), (24, 16, 3, 3), dict()
+        # 8x10 output: P % 8 == 0 takes the 16-byte Y/Z epilogue on the tensor-core route
+        xs, ws, extra = (2, 16, 8, 10), (24, 16, 3, 3), dict()
     attrs = dict(pads=[1, 1, 1, 1], activation=act, activation_params=params, **extra)
     x, w, b, z = inputs(500, "f16", xs, ws, True, True, attrs, wscale=0.8 / math.sqrt(9))
     compare("f16", x, w, b, z, attrs, route=route, what=f"act {act}")
