@@ -54,7 +54,8 @@ class FusedConvPlan:
                  has_bias: bool = False, has_z: bool = False, group: int = 1, strides=None,
                  dilations=None, pads=None, auto_pad: str = "NOTSET", kernel_shape=None,
                  activation: Optional[str] = None, activation_params=None, device: int = -1,
-                 route: str = "auto", split_k: int = 0, tile_n: int = 0, z_shape=None):
+                 route: str = "auto", split_k: int = 0, tile_n: int = 0, z_shape=None,
+                 a_path: str = "auto"):
         lib = _lib.load()
         self._lib = lib
         self._ptr = ctypes.c_void_p()
@@ -84,7 +85,8 @@ class FusedConvPlan:
                               dilations=dilations, pads=pads, auto_pad=auto_pad,
                               kernel_shape=kernel_shape, activation=activation,
                               activation_params=activation_params)
-        opts = _lib.FconvOptions(ROUTES[route], int(split_k), int(tile_n))
+        opts = _lib.FconvOptions(ROUTES[route], int(split_k), int(tile_n),
+                                 {"auto": 0, "gather": 1, "tma": 2}[a_path])
         _check(lib.fconv_plan_create_ex(ctypes.byref(desc), device, ctypes.byref(opts),
                                         ctypes.byref(self._ptr)), "fconv_plan_create")
         ys = (ctypes.c_int64 * 5)()
@@ -169,12 +171,12 @@ def plan_for(x, w, b=None, z=None, **attrs) -> FusedConvPlan:
 def fused_conv(x, w, b=None, z=None, *, group: int = 1, strides=None, dilations=None,
                pads=None, auto_pad: str = "NOTSET", kernel_shape=None,
                activation: Optional[str] = None, activation_params=None, out=None,
-               route: str = "auto", split_k: int = 0, tile_n: int = 0):
+               route: str = "auto", split_k: int = 0, tile_n: int = 0, a_path: str = "auto"):
     """Y = act(conv(X, W) + B + Z) on CUDA tensors (the operator's ONNX-style attributes)."""
     if not x.is_cuda:
         raise ValueError("fused_conv runs on CUDA tensors only")
     p = plan_for(x, w, b, z, group=group, strides=strides, dilations=dilations, pads=pads,
                  auto_pad=auto_pad, kernel_shape=kernel_shape, activation=activation,
                  activation_params=activation_params, route=route, split_k=split_k,
-                 tile_n=tile_n)
+                 tile_n=tile_n, a_path=a_path)
     return p.run(x, w, b, z, y=out)

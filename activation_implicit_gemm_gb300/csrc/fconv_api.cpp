@@ -178,7 +178,8 @@ void plan_igemm(fconv_plan* p, const fconv_options* o) {
   IgemmConfig& c = p->igemm;
   c.tile_n = (o && o->tile_n) ? o->tile_n : pick_tile_n(g.Mg);
   c.stages = igemm_tc_stages(c.tile_n);
-  const long long rows = ((long long)g.N * g.P + 127) / 128;
+  c.a_path = o ? o->a_path : 0;
+  const long long rows = igemm_tc_mtiles(g, c.a_path);
   const long long tiles = rows * ((g.Mg + c.tile_n - 1) / c.tile_n) * g.G;
   const int chunks = (g.Kg + 63) / 64;
   int split = 1;
@@ -230,6 +231,9 @@ fconv_status create(const fconv_desc* d, int device, const fconv_options* o, fco
              want != FCONV_ROUTE_IGEMM_TC) {
     st = FCONV_E_UNSUPPORTED;
   }
+  if (st == FCONV_OK && route == FCONV_ROUTE_IGEMM_TC && o &&
+      (o->a_path < 0 || o->a_path > 2 || (o->a_path == 2 && !igemm_tc_tma_capable(p->g))))
+    st = FCONV_E_UNSUPPORTED;
   if (st == FCONV_OK && route == FCONV_ROUTE_IGEMM_TC && o && o->tile_n &&
       (o->tile_n < 16 || o->tile_n > 256 || (o->tile_n & (o->tile_n - 1)) != 0))
     st = FCONV_E_UNSUPPORTED;

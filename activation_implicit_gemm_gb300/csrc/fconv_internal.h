@@ -44,6 +44,7 @@ struct IgemmConfig {
   int split_k;     // number of K splits (>= 1)
   int stages;      // shared-memory pipeline depth (even)
   long long grid;  // persistent CTAs (one per SM at most)
+  int a_path;      // 0 auto, 1 in-kernel gather of A, 2 TMA boxes of repacked X
 };
 
 // Launchers: return cudaError_t as int (0 = success).
@@ -55,6 +56,8 @@ bool depthwise_supported(const ConvGeom& g);
 int igemm_tc_stages(int tile_n);
 size_t igemm_tc_smem_bytes(int tile_n, int stages);
 size_t igemm_tc_workspace_bytes(const ConvGeom& g, const IgemmConfig& c);
+long long igemm_tc_mtiles(const ConvGeom& g, int a_path);  // pixel tiles of the A operand
+bool igemm_tc_tma_capable(const ConvGeom& g);             // TMA-fed A path possible
 
 // Device error word (set by kernels whose bounded waits gave up). Reads and clears.
 int read_and_clear_device_error(void* stream, unsigned* value);

@@ -11,7 +11,9 @@
 //             (0 outside X),   B[m, k] = W[g*Mg + m, ci, kz, ky, kx]
 // The K order is a free choice as long as A and B agree. With C/group a multiple of 8
 // the kernel uses k = tap*Cg + ci ("channel-inner"): every 8-wide piece of a row is 8
-// channels of one tap, so its validity is one test and its addresses one stride apart.
+// channels of one tap, so its validity is one test and its addresses one stride apart;
+// with C/group a multiple of 64 it uses (64-channel block, tap, channel), so that all
+// taps of a block reuse the same slab of X from L1.
 // The weights are then read from a copy in that order (prep_weights_kernel, into the
 // workspace); otherwise k = ci*KV + tap, W's own order.
 //
@@ -256,10 +258,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int k0 = (un.c_begin + i) * kBK;
         uint32_t v[64];
         if (CHAN && (g.Cg % kBK) == 0) {
-          // the whole chunk is 64 channels of one tap: one validity test, 64 loads one
-          // channel plane apart, all in flight before any store
-          const int tap = k0 / g.Cg;
-          const int ci = k0 - tap * g.Cg;
+          // K order (64-channel block, tap, channel): the chunk is 64 channels of one tap,
+          // and the taps of a block follow each other, so the block's slab of X stays in
+          // L1 across them. One validity test, 64 loads one channel plane apart, all in
+          // flight before any store.
+          const int chunk = un.c_begin + i;
+          const int cb = chunk / g.KV;
+          const int tap = chunk - cb * g.KV;
+          const int ci = cb * kBK;
           const int2 ti = tab[tap];
           const bool ok = ((mz >> (ti.y & 0xff)) & (my >> ((ti.y >> 8) & 0xff)) & (mx >> (ti.y >> 16))) & 1u;
           if (ok) {
@@ -495,6 +501,324 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+
+// ============================================================================
+// TMA-fed variant (C/group a multiple of 64). X is first repacked into blocks of 64
+// channels, channels innermost: Xb[c/64][n][d][h][w][64] (pack_x_kernel). A tile of
+// output pixels is a box (Nb images x Dt x Ht x Wt, at most 128 pixels); for a chunk
+// (64-channel block cb, tap t) its A operand is one 5-D TMA box of Xb at
+// (0, ow0*sW - pW + kx*dW, oh0*sH - pH + ky*dH, od0*sD - pD + kz*dD, (g*Cg/64 + cb)*N + n0)
+// with element strides (1, sW, sH, sD, 1): TMA applies stride, dilation and the zero
+// padding, and writes the 128-byte-swizzled K-major rows the MMA reads. The weights come
+// in the same (block, tap, channel) order. No thread touches the operands.
+//   warps 0-7  epilogue (two warps per TMEM lane quarter, alternate 16-column groups)
+//   warp 8     TMEM allocation + MMA issue
+//   warp 9     TMA producer (A and B of every chunk on one full barrier)
+// ============================================================================
+constexpr int kTmaWarps = 10;
+constexpr int kTmaThreads = kTmaWarps * 32;
+constexpr int kTmaEpiWarps = 8;
+constexpr int kTmaMmaWarp = 8;
+constexpr int kTmaLoadWarp = 9;
+
+struct TmaArgs {
+  const __half* b;
+  const __half* z;
+  __half* y;
+  float* part;
+  int stages;
+  int chunks, chunks_per_split, split, ntiles, cbg;
+  int Nb, Dt, Ht, Wt, nTd, nTh, nTw;
+  int rows;            // Nb*Dt*Ht*Wt <= 128
+  int vec;             // 8-row groups are 16-byte aligned, contiguous runs of Y
+  uint32_t a_bytes;
+  long long units;
+};
+
+struct TmaUnit {
+  int n0, od0, oh0, ow0;
+  int grp, ct, sp, c_begin, nk;
+};
+
+__device__ __forceinline__ TmaUnit decode_tma_unit(long long u, const TmaArgs& a, int G) {
+  TmaUnit t;
+  t.sp = (int)(u % a.split);
+  long long r = u / a.split;
+  const int gct = (int)(r % ((long long)G * a.ntiles));
+  long long rt = r / ((long long)G * a.ntiles);
+  t.grp = gct / a.ntiles;
+  t.ct = gct - t.grp * a.ntiles;
+  const int tw = (int)(rt % a.nTw); rt /= a.nTw;
+  const int th = (int)(rt % a.nTh); rt /= a.nTh;
+  const int td = (int)(rt % a.nTd); rt /= a.nTd;
+  t.n0 = (int)rt * a.Nb;
+  t.od0 = td * a.Dt;
+  t.oh0 = th * a.Ht;
+  t.ow0 = tw * a.Wt;
+  t.c_begin = t.sp * a.chunks_per_split;
+  t.nk = min(a.chunks_per_split, a.chunks - t.c_begin);
+  return t;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    igemm_tma_kernel(const ConvGeom g, const TmaArgs a, const __grid_constant__ CUtensorMap tmap_x,
+                     const __grid_constant__ CUtensorMap tmap_w) {
+  constexpr uint32_t kAccCols = BN < 32 ? 32 : BN;
+  constexpr uint32_t kTmemCols = 2 * kAccCols;
+  constexpr uint32_t kABytes = kBM * kBK * 2;
+  constexpr uint32_t kBBytes = BN * kBK * 2;
+  constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  constexpr uint32_t kIdesc = ptx::idesc_f16_f32(kBM, BN);
+
+  extern __shared__ uint8_t dsmem[];
+  __shared__ SharedCtl ctl;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const uint32_t base = (ptx::smem_addr(dsmem) + 1023u) & ~1023u;
+  const int S = a.stages;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(ptx::smem_addr(&ctl.full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl.empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(ptx::smem_addr(&ctl.acc_full[b]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl.acc_empty[b]), kTmaEpiWarps);
+    }
+    ptx::mbar_init(ptx::smem_addr(&ctl.drain), 1);
+    ctl.abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kTmaMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_addr(&ctl.tmem_base), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == kTmaLoadWarp && lane == 0) {
+    ptx::prefetch_tmap(&tmap_x);
+    ptx::prefetch_tmap(&tmap_w);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  volatile int* abort_flag = &ctl.abort_flag;
+
+  if (warp == kTmaLoadWarp) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (long long u = blockIdx.x; u < a.units; u += gridDim.x) {
+        if (*abort_flag) break;
+        const TmaUnit un = decode_tma_unit(u, a, g.G);
+        const int row0 = un.grp * g.Mg + un.ct * BN;
+        bool stop = false;
+        for (int i = 0; i < un.nk; ++i, ++it) {
+          const int s = (int)(it % (uint32_t)S);
+          if (it >= (uint32_t)S &&
+              !bounded_wait(ptx::smem_addr(&ctl.empty[s]), ((it / S) - 1) & 1, abort_flag)) {
+            stop = true;
+            break;
+          }
+          const int chunk = un.c_begin + i;
+          const int cb = chunk / g.KV;
+          const int tap = chunk - cb * g.KV;
+          const int kx = tap % g.KW, ky = (tap / g.KW) % g.KH, kz = tap / (g.KW * g.KH);
+          const uint32_t bar = ptx::smem_addr(&ctl.full[s]);
+          const uint32_t abase = base + (uint32_t)s * kStageBytes;
+          ptx::mbar_arrive_expect_tx(bar, a.a_bytes + kBBytes);
+          ptx::tma_load_5d(abase, &tmap_x, 0, un.ow0 * g.sW - g.pW + kx * g.dW,
+                           un.oh0 * g.sH - g.pH + ky * g.dH, un.od0 * g.sD - g.pD + kz * g.dD,
+                           (un.grp * a.cbg + cb) * g.N + un.n0, bar);
+          ptx::tma_load_2d(abase + kABytes, &tmap_w, chunk * kBK, row0, bar);
+        }
+        if (stop) break;
+      }
+    }
+  } else if (warp == kTmaMmaWarp) {
+    // ================================================================ MMA issue
+    if (lane == 0) {
+      uint32_t it = 0, tcount = 0;
+      for (long long u = blockIdx.x; u < a.units; u += gridDim.x, ++tcount) {
+        if (*abort_flag) break;
+        const TmaUnit un = decode_tma_unit(u, a, g.G);
+        const uint32_t b = tcount & 1u;
+        if (tcount >= 2 &&
+            !bounded_wait(ptx::smem_addr(&ctl.acc_empty[b]), ((tcount >> 1) - 1) & 1, abort_flag))
+          break;
+        ptx::tc_fence_after();
+        const uint32_t dacc = tmem + b * kAccCols;
+        bool stop = false;
+        for (int i = 0; i < un.nk; ++i, ++it) {
+          const int s = (int)(it % (uint32_t)S);
+          if (!bounded_wait(ptx::smem_addr(&ctl.full[s]), (it / S) & 1, abort_flag)) {
+            stop = true;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t abase = base + (uint32_t)s * kStageBytes;
+          const uint32_t bbase = abase + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            ptx::mma_f16(dacc, ptx::desc_sw128(abase + kk * 32), ptx::desc_sw128(bbase + kk * 32),
+                         kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(ptx::smem_addr(&ctl.empty[s]));
+        }
+        if (stop) break;
+        ptx::mma_commit(ptx::smem_addr(&ctl.acc_full[b]));
+      }
+      ptx::mma_commit(ptx::smem_addr(&ctl.drain));
+      bounded_wait(ptx::smem_addr(&ctl.drain), 0, abort_flag);
+    }
+  } else {
+    // ================================================================ epilogue (warps 0-7)
+    const int q = warp & 3;      // TMEM lane quarter
+    const int half = warp >> 2;  // which alternate 16-column groups
+    const int r = q * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    const uint32_t yst = base + (uint32_t)S * kStageBytes + (uint32_t)warp * 2048u;
+    const uint32_t zst = yst + 1024u;
+    // this row's place in the pixel box
+    const int wt = r % a.Wt;
+    const int ht = (r / a.Wt) % a.Ht;
+    const int dt = (r / (a.Wt * a.Ht)) % a.Dt;
+    const int nb = r / (a.Wt * a.Ht * a.Dt);
+    // the 8-row group this lane moves in the vector path
+    const int gr = q * 32 + (lane & 3) * 8;
+    const int gwt = gr % a.Wt, ght = (gr / a.Wt) % a.Ht, gdt = (gr / (a.Wt * a.Ht)) % a.Dt;
+    const int gnb = gr / (a.Wt * a.Ht * a.Dt);
+    const long long NP = (long long)g.N * g.P;
+    uint32_t tcount = 0;
+    for (long long u = blockIdx.x; u < a.units; u += gridDim.x, ++tcount) {
+      if (*abort_flag) break;
+      const TmaUnit un = decode_tma_unit(u, a, g.G);
+      const uint32_t b = tcount & 1u;
+      if (!bounded_wait(ptx::smem_addr(&ctl.acc_full[b]), (tcount >> 1) & 1, abort_flag)) break;
+      ptx::tc_fence_after();
+      const int n = un.n0 + nb, od = un.od0 + dt, oh = un.oh0 + ht, ow = un.ow0 + wt;
+      const bool row_ok = r < a.rows && n < g.N && od < g.OD && oh < g.OH && ow < g.OW;
+      const long long obase =
+          row_ok ? (long long)n * g.M * g.P + ((long long)od * g.OH + oh) * g.OW + ow : 0;
+      const int gn = un.n0 + gnb, god = un.od0 + gdt, goh = un.oh0 + ght, gow = un.ow0 + gwt;
+      const bool grp_ok =
+          gr < a.rows && gn < g.N && god < g.OD && goh < g.OH && gow < g.OW;
+      const long long gpix = ((long long)god * g.OH + goh) * g.OW + gow;
+      const int mc0 = un.ct * BN;
+#pragma unroll 1
+      for (int c0 = half * 16; c0 < BN; c0 += 32) {
+        float v[16];
+        __syncwarp();
+        ptx::tmem_ld16(lane_base + b * kAccCols + (uint32_t)c0, v);
+        const int mcb = mc0 + c0;
+        const int nvalid = min(16, g.Mg - mcb);
+        if (nvalid <= 0) continue;
+        const int m0 = un.grp * g.Mg + mcb;
+        const bool hz = a.z != nullptr, hb = a.b != nullptr;
+        uint32_t zr[16], br[16];
+        if (a.part) {
+          if (!row_ok) continue;
+          float* pp = a.part + (long long)un.sp * NP * g.M + obase + (long long)m0 * g.P;
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            if (jj < nvalid) pp[(long long)jj * g.P] = v[jj];
+          continue;
+        }
+        if (a.vec) {
+          if (hz) {
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const int ch = (lane >> 2) + 8 * t;
+              uint4 zv = make_uint4(0, 0, 0, 0);
+              if (grp_ok && ch < nvalid)
+                zv = ptx::ldg_nc_v4(a.z + (((long long)gn * g.M + m0 + ch) * g.P + gpix));
+              ptx::st_shared_v4(zst + ch * 64 + (lane & 3) * 16, zv.x, zv.y, zv.z, zv.w);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) zr[jj] = ptx::ld_shared_u16(zst + jj * 64 + lane * 2);
+          }
+          if (hb) {
+            const uint32_t bl = ptx::ld1_u16(a.b + m0 + (lane & 15), (lane & 15) < nvalid ? 1u : 0u);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) br[jj] = __shfl_sync(0xffffffffu, bl, jj);
+          }
+#define FCONV_EPI16S(ACT) epi_stage16<ACT>(v, zr, br, hz, hb, yst + lane * 2, g.alpha, g.beta)
+          FCONV_ACT_SWITCH(g.act, FCONV_EPI16S)
+#undef FCONV_EPI16S
+          __syncwarp();
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int ch = (lane >> 2) + 8 * t;
+            if (grp_ok && ch < nvalid) {
+              const uint4 yv = ptx::ld_shared_v4(yst + ch * 64 + (lane & 3) * 16);
+              ptx::st_global_v4(a.y + (((long long)gn * g.M + m0 + ch) * g.P + gpix), yv);
+            }
+          }
+          __syncwarp();
+          continue;
+        }
+        if (!row_ok) continue;
+        const long long yb = obase + (long long)m0 * g.P;
+        if (hz) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            zr[jj] = ptx::ld1_u16(a.z + yb + (long long)jj * g.P, jj < nvalid ? 1u : 0u);
+        }
+        if (hb) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) br[jj] = ptx::ld1_u16(a.b + m0 + jj, jj < nvalid ? 1u : 0u);
+        }
+        __half* yp = a.y + yb;
+#define FCONV_EPI16(ACT) epi_store16<ACT>(v, zr, br, hz, hb, nvalid, yp, g.P, g.alpha, g.beta)
+        FCONV_ACT_SWITCH(g.act, FCONV_EPI16)
+#undef FCONV_EPI16
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl.acc_empty[b]));
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kTmaMmaWarp) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// X (N, C, spatial S) -> Xb[c/64][n][s][64]: 64 x 64 tiles transposed through shared
+// memory, coalesced on both sides.
+__global__ void __launch_bounds__(256) pack_x_kernel(const uint16_t* __restrict__ x,
+                                                     uint16_t* __restrict__ xb, int N, int C,
+                                                     long long S) {
+  __shared__ uint16_t t[64][66];
+  const long long s0 = (long long)blockIdx.x * 64;
+  const int cb = blockIdx.y;
+  const int n = blockIdx.z;
+  const uint16_t* src = x + ((long long)n * C + (long long)cb * 64) * S + s0;
+  for (int i = threadIdx.x; i < 64 * 64; i += 256) {
+    const int c = i >> 6, p = i & 63;
+    t[c][p] = (s0 + p < S) ? src[(long long)c * S + p] : (uint16_t)0;
+  }
+  __syncthreads();
+  uint16_t* dst = xb + (((long long)cb * N + n) * S + s0) * 64;
+  for (int j = threadIdx.x; j < 64 * 8; j += 256) {
+    const int p = j >> 3, part = j & 7;
+    if (s0 + p >= S) continue;
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      w[e] = (uint32_t)t[8 * part + 2 * e][p] | ((uint32_t)t[8 * part + 2 * e + 1][p] << 16);
+    *reinterpret_cast<uint4*>(dst + (long long)p * 64 + 8 * part) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 // Weights in the GEMM's K order, zero padded to kpad columns: wp[m][k'] for k' < kpad.
 __global__ void __launch_bounds__(256) prep_weights_kernel(const uint16_t* __restrict__ w,
                                                            uint16_t* __restrict__ wp, int M,
@@ -508,7 +832,12 @@ __global__ void __launch_bounds__(256) prep_weights_kernel(const uint16_t* __res
     uint16_t v = 0;
     if (k < Kg) {
       int src = k;
-      if (chan) {
+      if (chan && (Cg % 64) == 0) {
+        // (64-channel block, tap, channel)
+        const int cb = k / (64 * KV), rem = k - cb * 64 * KV;
+        const int tap = rem / 64, ci = cb * 64 + (rem - tap * 64);
+        src = ci * KV + tap;
+      } else if (chan) {
         const int tap = k / Cg, ci = k - tap * Cg;
         src = ci * KV + tap;
       }
@@ -560,6 +889,37 @@ EncodeTiledFn encode_fn() {
 
 bool channel_inner(const ConvGeom& g) { return (g.Cg % 8) == 0; }
 
+// Pixel box of the TMA-fed kernel.
+struct TmaShape {
+  bool ok;
+  int Nb, Dt, Ht, Wt, rows, vec;
+  long long mtiles;
+};
+
+TmaShape tma_shape(const ConvGeom& g) {
+  TmaShape t{};
+  t.ok = (g.Cg % kBK) == 0 && g.sD <= 8 && g.sH <= 8 && g.sW <= 8 &&
+         (long long)g.C * g.N <= 0x7fffffffLL / 64;
+  if (!t.ok) return t;
+  t.Wt = min(g.OW, min(128, 256 / g.sW));
+  t.Ht = min(g.OH, min(128 / t.Wt, 256 / g.sH));
+  t.Dt = min(g.OD, min(128 / (t.Wt * t.Ht), 256 / g.sD));
+  const bool whole = t.Wt == g.OW && t.Ht == g.OH && t.Dt == g.OD;
+  t.Nb = whole ? min(g.N, 128 / (t.Wt * t.Ht * t.Dt)) : 1;
+  t.rows = t.Nb * t.Dt * t.Ht * t.Wt;
+  t.mtiles = (long long)((g.N + t.Nb - 1) / t.Nb) * ((g.OD + t.Dt - 1) / t.Dt) *
+             ((g.OH + t.Ht - 1) / t.Ht) * ((g.OW + t.Wt - 1) / t.Wt);
+  t.vec = (g.P % 8 == 0) && ((t.Wt % 8 == 0 && g.OW % t.Wt == 0) || whole);
+  // 8-pixel groups never straddle the 32-row lane quarters: rows is a multiple of 8 or
+  // the groups past `rows` are simply invalid
+  return t;
+}
+
+bool use_tma(const ConvGeom& g, int a_path) {
+  if (a_path == 1) return false;
+  return tma_shape(g).ok;
+}
+
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 template <int BN, bool CHAN>
@@ -586,6 +946,30 @@ int launch_bn(const ConvGeom& g, const IgemmConfig& c, const TcArgs& ta, const C
   }
 }
 
+template <int BN>
+int launch_tma_t(const ConvGeom& g, const IgemmConfig& c, const TmaArgs& t, const CUtensorMap& tx,
+                 const CUtensorMap& tw, cudaStream_t s) {
+  const size_t smem = (size_t)c.stages * (size_t)(kBM * kBK * 2 + BN * kBK * 2) + 1024 +
+                      (size_t)kTmaEpiWarps * 2048;
+  cudaError_t e = cudaFuncSetAttribute(igemm_tma_kernel<BN>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return (int)e;
+  igemm_tma_kernel<BN><<<(unsigned)c.grid, kTmaThreads, smem, s>>>(g, t, tx, tw);
+  return (int)cudaGetLastError();
+}
+
+int launch_reduce(const ConvGeom& g, const IgemmConfig& c, const float* part, const __half* b,
+                  const __half* z, __half* y, cudaStream_t s) {
+  const long long total = (long long)g.N * g.M * g.P;
+  long long blocks = (total + 255) / 256;
+  if (blocks > 152LL * 32) blocks = 152LL * 32;
+#define FCONV_REDUCE(ACT)                                                                    \
+  splitk_reduce_kernel<ACT><<<(unsigned)blocks, 256, 0, s>>>(g, part, c.split_k, b, z, y, total)
+  FCONV_ACT_SWITCH(g.act, FCONV_REDUCE)
+#undef FCONV_REDUCE
+  return (int)cudaGetLastError();
+}
+
 }  // namespace
 
 int igemm_tc_stages(int tile_n) {
@@ -598,7 +982,7 @@ int igemm_tc_stages(int tile_n) {
 
 size_t igemm_tc_smem_bytes(int tile_n, int stages) {
   // operand ring + 1 KB alignment slack + the epilogue warps' Y/Z staging tiles
-  return (size_t)stages * (size_t)(kBM * kBK * 2 + tile_n * kBK * 2) + 1024 + 4 * 2048;
+  return (size_t)stages * (size_t)(kBM * kBK * 2 + tile_n * kBK * 2) + 1024 + 8 * 2048;
 }
 
 // Weight copy in GEMM order (when W itself cannot be read by TMA in that order).
@@ -613,10 +997,21 @@ static size_t prep_bytes(const ConvGeom& g) {
   return needs_prep(g) ? round_up((size_t)g.M * kpad_of(g) * 2, 1024) : 0;
 }
 
+static size_t pack_bytes(const ConvGeom& g, const IgemmConfig& c) {
+  return use_tma(g, c.a_path) ? round_up((size_t)g.N * g.C * (size_t)g.IS * 2, 1024) : 0;
+}
+
 size_t igemm_tc_workspace_bytes(const ConvGeom& g, const IgemmConfig& c) {
-  size_t b = prep_bytes(g);
+  size_t b = prep_bytes(g) + pack_bytes(g, c);
   if (c.split_k > 1) b += (size_t)c.split_k * (size_t)g.N * (size_t)g.M * (size_t)g.P * 4;
   return b;
+}
+
+bool igemm_tc_tma_capable(const ConvGeom& g) { return tma_shape(g).ok; }
+
+long long igemm_tc_mtiles(const ConvGeom& g, int a_path) {
+  if (use_tma(g, a_path)) return tma_shape(g).mtiles;
+  return ((long long)g.N * g.P + kBM - 1) / kBM;
 }
 
 bool igemm_tc_supported(const ConvGeom& g) {
@@ -653,6 +1048,15 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
     if (e != cudaSuccess) return (int)e;
     wmat = wp;
   }
+  const bool tma = use_tma(g, c.a_path);
+  const size_t xb_bytes = pack_bytes(g, c);
+  if (tma) {
+    const long long S = g.IS;
+    dim3 pg((unsigned)((S + 63) / 64), (unsigned)(g.C / 64), (unsigned)g.N);
+    pack_x_kernel<<<pg, 256, 0, s>>>((const uint16_t*)a.x, (uint16_t*)(ws + pb), g.N, g.C, S);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
+  }
   const int wcols = pb ? kpad : g.Kg;
   CUtensorMap tm;
   std::memset(&tm, 0, sizeof(tm));
@@ -665,12 +1069,60 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return (int)cudaErrorInvalidValue;
 
+  float* part = c.split_k > 1 ? (float*)(ws + pb + xb_bytes) : nullptr;
+  if (tma) {
+    const TmaShape sh = tma_shape(g);
+    CUtensorMap tx;
+    std::memset(&tx, 0, sizeof(tx));
+    const cuuint64_t cbn = (cuuint64_t)(g.C / 64) * (cuuint64_t)g.N;
+    cuuint64_t xdims[5] = {64, (cuuint64_t)g.IW, (cuuint64_t)g.IH, (cuuint64_t)g.ID, cbn};
+    cuuint64_t xstr[4] = {128, (cuuint64_t)g.IW * 128, (cuuint64_t)g.IH * g.IW * 128,
+                          (cuuint64_t)g.ID * g.IH * g.IW * 128};
+    cuuint32_t xbox[5] = {64, (cuuint32_t)(sh.Wt * g.sW), (cuuint32_t)(sh.Ht * g.sH),
+                          (cuuint32_t)(sh.Dt * g.sD), (cuuint32_t)sh.Nb};
+    cuuint32_t xes[5] = {1, (cuuint32_t)g.sW, (cuuint32_t)g.sH, (cuuint32_t)g.sD, 1};
+    cr = enc(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5, (void*)(ws + pb), xdims, xstr, xbox, xes,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return (int)cudaErrorInvalidValue;
+    TmaArgs t;
+    t.b = (const __half*)a.b;
+    t.z = (const __half*)a.z;
+    t.y = (__half*)a.y;
+    t.part = part;
+    t.stages = c.stages;
+    t.chunks = (g.Kg + kBK - 1) / kBK;
+    t.chunks_per_split = (t.chunks + c.split_k - 1) / c.split_k;
+    t.split = c.split_k;
+    t.ntiles = (g.Mg + c.tile_n - 1) / c.tile_n;
+    t.cbg = g.Cg / 64;
+    t.Nb = sh.Nb; t.Dt = sh.Dt; t.Ht = sh.Ht; t.Wt = sh.Wt;
+    t.nTd = (g.OD + sh.Dt - 1) / sh.Dt;
+    t.nTh = (g.OH + sh.Ht - 1) / sh.Ht;
+    t.nTw = (g.OW + sh.Wt - 1) / sh.Wt;
+    t.rows = sh.rows;
+    t.vec = sh.vec;
+    t.a_bytes = (uint32_t)sh.rows * 128u;
+    t.units = sh.mtiles * g.G * t.ntiles * c.split_k;
+    int err;
+    switch (c.tile_n) {
+      case 16: err = launch_tma_t<16>(g, c, t, tx, tm, s); break;
+      case 32: err = launch_tma_t<32>(g, c, t, tx, tm, s); break;
+      case 64: err = launch_tma_t<64>(g, c, t, tx, tm, s); break;
+      case 128: err = launch_tma_t<128>(g, c, t, tx, tm, s); break;
+      case 256: err = launch_tma_t<256>(g, c, t, tx, tm, s); break;
+      default: return (int)cudaErrorInvalidValue;
+    }
+    if (err != 0 || c.split_k <= 1) return err;
+    return launch_reduce(g, c, part, (const __half*)a.b, (const __half*)a.z, (__half*)a.y, s);
+  }
+
   TcArgs ta;
   ta.x = (const uint16_t*)a.x;
   ta.b = (const __half*)a.b;
   ta.z = (const __half*)a.z;
   ta.y = (__half*)a.y;
-  ta.part = c.split_k > 1 ? (float*)(ws + pb) : nullptr;
+  ta.part = part;
   ta.stages = c.stages;
   ta.chunks = (g.Kg + kBK - 1) / kBK;
   ta.chunks_per_split = (ta.chunks + c.split_k - 1) / c.split_k;
@@ -680,15 +1132,7 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
   ta.units = ta.row_tiles * g.G * ta.ntiles * c.split_k;
   const int err = chan ? launch_bn<true>(g, c, ta, tm, s) : launch_bn<false>(g, c, ta, tm, s);
   if (err != 0 || c.split_k <= 1) return err;
-  const long long total = (long long)g.N * g.M * g.P;
-  long long blocks = (total + 255) / 256;
-  if (blocks > 152LL * 32) blocks = 152LL * 32;
-#define FCONV_REDUCE(ACT)                                                                  \
-  splitk_reduce_kernel<ACT><<<(unsigned)blocks, 256, 0, s>>>(g, ta.part, c.split_k, ta.b, ta.z, \
-                                                             ta.y, total)
-  FCONV_ACT_SWITCH(g.act, FCONV_REDUCE)
-#undef FCONV_REDUCE
-  return (int)cudaGetLastError();
+  return launch_reduce(g, c, part, ta.b, ta.z, ta.y, s);
 }
 
 int read_and_clear_device_error(void* stream, unsigned* value) {

@@ -252,5 +252,15 @@ __device__ __forceinline__ void st_shared_pack8(uint32_t addr, const uint32_t* v
       : "memory");
 }
 
+// 5-D tiled TMA load (c0 innermost).
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tmap, int c0, int c1, int c2,
+                                            int c3, int c4, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"((uint64_t)tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
+      : "memory");
+}
+
 }  // namespace ptx
 }  // namespace fconv

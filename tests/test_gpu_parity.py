@@ -58,10 +58,11 @@ def gpu_run(plan: FusedConvPlan, xd, wd, bd, zd, dtype) -> np.ndarray:
     return y.double().cpu().numpy()
 
 
-def compare(dtype, x, w, b, z, attrs, route="auto", split_k=0, tile_n=0, what=""):
+def compare(dtype, x, w, b, z, attrs, route="auto", split_k=0, tile_n=0, what="",
+            a_path="auto"):
     dt = _lib.F16 if dtype == "f16" else _lib.F32
     plan = FusedConvPlan(dt, x.shape, w.shape, has_bias=b is not None, has_z=z is not None,
-                         route=route, split_k=split_k, tile_n=tile_n, **attrs)
+                         route=route, split_k=split_k, tile_n=tile_n, a_path=a_path, **attrs)
     y = gpu_run(plan, to_dev(x), to_dev(w), to_dev(b), to_dev(z), dtype)
     ref, absacc = oracle.fused_conv(x, w, b, z, **attrs)
     pre = None
@@ -107,6 +108,38 @@ def test_tc_vector_epilogue_ragged(tile_n, split_k):
     x, w, b, z = inputs(13, "f16", (3, 16, 8, 8), (40, 16, 3, 3), True, True, attrs)
     compare("f16", x, w, b, z, attrs, route="igemm_tc", tile_n=tile_n, split_k=split_k,
             what="vector epilogue")
+
+
+TMA_CASES = [
+    # (x_shape, w_shape, attrs, bias, z, tile_n, split_k): C/group % 64 == 0, so X is
+    # repacked in 64-channel blocks and A arrives by TMA boxes
+    ((3, 64, 8, 8), (40, 64, 3, 3), dict(pads=[1, 1, 1, 1]), True, True, 0, 0),        # whole images
+    ((2, 64, 13, 11), (72, 64, 3, 3), dict(pads=[1, 0, 2, 1]), True, True, 0, 0),      # ragged box
+    ((2, 128, 16, 16), (48, 128, 3, 3), dict(pads=[1, 1, 1, 1], activation="Gelu"), False, True, 64, 2),
+    ((2, 64, 20, 20), (64, 64, 2, 2), dict(strides=[2, 2]), True, False, 0, 0),        # stride 2
+    ((1, 64, 17, 19), (32, 64, 3, 3), dict(dilations=[2, 3], pads=[2, 3, 2, 3]), True, True, 32, 1),
+    ((2, 64, 300), (64, 64, 5), dict(dilations=[2], auto_pad="SAME_UPPER"), True, True, 0, 0),
+    ((1, 64, 6, 9, 10), (16, 64, 3, 3, 3), dict(strides=[2, 2, 2], auto_pad="SAME_LOWER"), True, True, 0, 0),
+    ((2, 128, 7, 9), (96, 64, 3, 3), dict(group=2, pads=[1, 1, 1, 1]), True, True, 0, 0),  # grouped
+    ((9, 256, 4, 4), (320, 256, 3, 3), dict(pads=[1, 1, 1, 1], activation="HardSwish"), False, True, 256, 0),
+    ((2, 64, 9, 9), (24, 64, 1, 1), dict(), True, False, 0, 0),                        # 1x1
+    ((2, 64, 12, 12), (16, 64, 3, 3), dict(strides=[3, 3], pads=[1, 1, 1, 1]), True, True, 16, 3),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(TMA_CASES)))
+def test_tc_tma_path(idx):
+    xs, ws, attrs, bias, zres, tile_n, split_k = TMA_CASES[idx]
+    x, w, b, z = inputs(300 + 10 * idx, "f16", xs, ws, bias, zres, attrs)
+    dt = _lib.F16
+    plan = FusedConvPlan(dt, x.shape, w.shape, has_bias=b is not None, has_z=z is not None,
+                         route="igemm_tc", a_path="tma", split_k=split_k, tile_n=tile_n, **attrs)
+    y = gpu_run(plan, to_dev(x), to_dev(w), to_dev(b), to_dev(z), "f16")
+    ref, absacc = oracle.fused_conv(x, w, b, z, **attrs)
+    check(y, ref, absacc, "f16", int(np.prod(w.shape[1:])), activation=attrs.get("activation"),
+          what=f"tma case {idx} tile={plan.tile_n} split={plan.split_k}")
+    # the same request through the in-kernel gather agrees too
+    compare("f16", x, w, b, z, attrs, route="igemm_tc", a_path="gather", what=f"gather case {idx}")
 
 
 TC_CASES = [
