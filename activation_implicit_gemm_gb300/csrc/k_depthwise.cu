@@ -72,58 +72,142 @@ __device__ __forceinline__ void store_run(const float (&acc)[VW], const T* __res
       y[o + j] = from_f32<T>(act_eval<ACT, sizeof(T) == 2>(acc[j] + zv[j], alpha, beta));
 }
 
-// Fast path: stride 1 and dilation 1 along W, KW known at compile time.
-template <typename T, int KW, int VW>
-__global__ void __launch_bounds__(kDwThreads) dw_kernel_fast(ConvGeom g, const T* __restrict__ x,
-                                                             const T* __restrict__ w,
-                                                             const T* __restrict__ b,
-                                                             const T* __restrict__ z,
-                                                             T* __restrict__ y, int band,
-                                                             int bands, int srows, int scols) {
-  extern __shared__ float smem[];
-  float* sw = smem;                       // KH*KW weights
-  float* sx = smem + g.KH * KW;           // staged input
-  const int plane = blockIdx.x / bands;   // n*C + c
-  const int bi = blockIdx.x - plane * bands;
+// + Z, activation and rounding of a 4 x 4 block (rows nr, columns nv valid): all Z
+// loads first, then the math, then the stores.
+template <int ACT, typename T>
+__device__ __forceinline__ void store_block4(const float (&acc)[4][4], const T* __restrict__ z,
+                                             T* __restrict__ y, long long o, int OW, int nr,
+                                             int nv, float alpha, float beta) {
+  float zv[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      zv[r][j] = (z && r < nr && j < nv) ? to_f32(z[o + (long long)r * OW + j]) : 0.0f;
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (r < nr && j < nv)
+        y[o + (long long)r * OW + j] =
+            from_f32<T>(act_eval<ACT, sizeof(T) == 2>(acc[r][j] + zv[r][j], alpha, beta));
+}
+
+// Fast path: stride 1 and dilation 1 on both axes, KH and KW known at compile time.
+// A CTA owns an output tile of TR x TC (both multiples of 4) of one (image, channel)
+// plane; each thread computes a 4 x 4 block of outputs from KH + 3 input rows of
+// KW + 3 values each, read as 16-byte vectors from the fp32 halo tile in shared memory
+// (column c of the tile holds input column c - 4 + ox0 - pW, so every vector read of a
+// thread starts 16-byte aligned). Weights live in registers; accumulation is fp32.
+template <typename T, int KH, int KW>
+__global__ void __launch_bounds__(256) dw_kernel_block(ConvGeom g, const T* __restrict__ x,
+                                                       const T* __restrict__ w,
+                                                       const T* __restrict__ b,
+                                                       const T* __restrict__ z,
+                                                       T* __restrict__ y, int TR, int TC,
+                                                       int tiles_r, int tiles_c, int pitch) {
+  extern __shared__ float sx[];  // (TR + KH - 1) rows x pitch floats
+  constexpr int WIN = 4 + KW - 1;
+  constexpr int WV = (WIN + 3 + 3) / 4;  // 16-byte vectors covering the window (+3 offset)
+  const int tiles = tiles_r * tiles_c;
+  const int plane = blockIdx.x / tiles;
+  const int tile = blockIdx.x - plane * tiles;
+  const int tr = tile / tiles_c, tc = tile - tr * tiles_c;
+  const int oy0 = tr * TR, ox0 = tc * TC;
   const int c = plane % g.C;
-  const int oh0 = bi * band;
-  const int nrows = min(band, g.OH - oh0);
-  const int row0 = oh0 * g.sH - g.pH;
   const T* xp = x + (long long)plane * g.IS;
-  for (int i = threadIdx.x; i < g.KH * KW; i += blockDim.x) sw[i] = to_f32(w[(long long)c * g.KH * KW + i]);
-  stage_input(g, xp, sx, row0, srows, scols);
-  __syncthreads();
+  const int srows = TR + KH - 1;
+  const int iy0 = oy0 - g.pH;          // input row of tile row 0
+  const int ixb = ox0 - g.pW - 4;      // input column of tile column 0
+  // zero the tile (padding), then copy the input rows it covers with 16-byte loads,
+  // four in flight per thread
+  for (int i = threadIdx.x * 4; i < srows * pitch; i += blockDim.x * 4)
+    *reinterpret_cast<float4*>(sx + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wr[KH * KW];
+#pragma unroll
+  for (int i = 0; i < KH * KW; ++i) wr[i] = to_f32(w[(long long)c * KH * KW + i]);
   const float bias = b ? to_f32(b[c]) : 0.0f;
-  const int runs_per_row = (g.OW + VW - 1) / VW;
-  const int runs = nrows * runs_per_row;
-  const long long ybase = (long long)plane * g.P;
-  for (int r = threadIdx.x; r < runs; r += blockDim.x) {
-    const int orow = r / runs_per_row;
-    const int ow0 = (r - orow * runs_per_row) * VW;
-    const int oh = oh0 + orow;
-    float acc[VW];
+  __syncthreads();
+  {
+    constexpr int VE = 16 / sizeof(T);                   // elements per 16-byte vector
+    const int lo = max(0, ixb), hi = min(g.IW, ixb + pitch);
+    const int r0 = max(0, -iy0), r1 = min(srows, g.IH - iy0);
+    const bool vec = (g.IW % VE) == 0 && (g.IS % VE) == 0;
+    if (vec && hi > lo && r1 > r0) {
+      const int v0 = lo / VE, v1 = (hi + VE - 1) / VE;   // vectors of input columns
+      const int nvr = v1 - v0;
+      const int total = (r1 - r0) * nvr;
+      for (int i0 = threadIdx.x; i0 < total; i0 += 4 * blockDim.x) {
+        uint4 buf[4];
 #pragma unroll
-    for (int j = 0; j < VW; ++j) acc[j] = bias;
-    const float* srow = sx + (orow * g.sH) * scols + ow0;
-    for (int ky = 0; ky < g.KH; ++ky) {
-      const float* s = srow + ky * g.dH * scols;
-      float win[VW + KW - 1];
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * blockDim.x;
+          if (i < total) {
+            const int rr = r0 + i / nvr, vv = v0 + i % nvr;
+            buf[u] = *reinterpret_cast<const uint4*>(xp + (long long)(iy0 + rr) * g.IW + vv * VE);
+          }
+        }
 #pragma unroll
-      for (int i = 0; i < VW + KW - 1; ++i) win[i] = (ow0 + i < scols) ? s[i] : 0.0f;
-      const float* wr = sw + ky * KW;
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * blockDim.x;
+          if (i < total) {
+            const int rr = r0 + i / nvr, vv = v0 + i % nvr;
+            const T* e = reinterpret_cast<const T*>(&buf[u]);
 #pragma unroll
-      for (int kx = 0; kx < KW; ++kx) {
-        const float wv = wr[kx];
-#pragma unroll
-        for (int j = 0; j < VW; ++j) acc[j] = fmaf(win[j + kx], wv, acc[j]);
+            for (int k = 0; k < VE; ++k) {
+              const int ix = vv * VE + k;
+              if (ix >= lo && ix < hi) sx[rr * pitch + (ix - ixb)] = to_f32(e[k]);
+            }
+          }
+        }
+      }
+    } else {
+      for (int i = threadIdx.x; i < (r1 - r0) * (hi - lo); i += blockDim.x) {
+        const int rr = r0 + i / (hi - lo), ix = lo + i % (hi - lo);
+        sx[rr * pitch + (ix - ixb)] = to_f32(xp[(long long)(iy0 + rr) * g.IW + ix]);
       }
     }
-    const long long o = ybase + (long long)oh * g.OW + ow0;
-    const int nv = min(VW, g.OW - ow0);
-#define FCONV_DW_STORE(ACT) store_run<ACT, T, VW>(acc, z, y, o, nv, g.alpha, g.beta)
-    FCONV_ACT_SWITCH(g.act, FCONV_DW_STORE)
-#undef FCONV_DW_STORE
   }
+  __syncthreads();
+
+  const int tcols = TC / 4;
+  const int ty = threadIdx.x / tcols, tx = threadIdx.x - ty * tcols;
+  if (ty * 4 >= TR) return;
+  const int oy = oy0 + ty * 4, ox = ox0 + tx * 4;
+  if (oy >= g.OH || ox >= g.OW) return;
+  float acc[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[r][j] = bias;
+  // tile column of output ox + j, tap kx: (ox + j + kx - pW) - ixb = tx*4 + 4 + j + kx
+  const float* base = sx + (ty * 4) * pitch + tx * 4 + 4;
+#pragma unroll
+  for (int ir = 0; ir < 4 + KH - 1; ++ir) {
+    float win[WV * 4];
+    const float4* rp = reinterpret_cast<const float4*>(base + ir * pitch);
+#pragma unroll
+    for (int q = 0; q < WV; ++q) {
+      const float4 f = rp[q];
+      win[4 * q] = f.x; win[4 * q + 1] = f.y; win[4 * q + 2] = f.z; win[4 * q + 3] = f.w;
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int ky = ir - r;
+      if (ky < 0 || ky >= KH) continue;
+#pragma unroll
+      for (int kx = 0; kx < KW; ++kx) {
+        const float wv = wr[ky * KW + kx];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[r][j] = fmaf(win[j + kx], wv, acc[r][j]);
+      }
+    }
+  }
+  const long long ybase = (long long)plane * g.P + (long long)oy * g.OW + ox;
+  const int nv = min(4, g.OW - ox), nr = min(4, g.OH - oy);
+#define FCONV_DW_STORE(ACT) store_block4<ACT, T>(acc, z, y, ybase, g.OW, nr, nv, g.alpha, g.beta)
+  FCONV_ACT_SWITCH(g.act, FCONV_DW_STORE)
+#undef FCONV_DW_STORE
 }
 
 // General path: any stride and dilation, one output per thread iteration.
@@ -174,19 +258,29 @@ int launch_dw_t(const ConvGeom& g, const ConvArgs& a, cudaStream_t s) {
   const T* b = (const T*)a.b;
   const T* z = (const T*)a.z;
   T* y = (T*)a.y;
-  const bool unit = g.sW == 1 && g.dW == 1;
-#define FCONV_DW_FAST(KWV)                                                                   \
-  if (unit && g.KW == KWV) {                                                                 \
-    auto k = dw_kernel_fast<T, KWV, 4>;                                                      \
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem);      \
-    k<<<(unsigned)blocks, kDwThreads, L.smem, s>>>(g, x, w, b, z, y, L.band, L.bands, L.srows, \
-                                                    L.scols);                                \
-    return (int)cudaGetLastError();                                                          \
+  const bool unit = g.sW == 1 && g.dW == 1 && g.sH == 1 && g.dH == 1;
+  if (unit && g.KH == g.KW && (g.KW == 3 || g.KW == 5 || g.KW == 7)) {
+    // output tile: TC columns (<= 64, a multiple of 4), TR rows, at most 256 threads
+    const int TC = min(64, (g.OW + 3) / 4 * 4);
+    int TR = min((g.OH + 3) / 4 * 4, (256 / (TC / 4)) * 4);
+    if (TR > 64) TR = 64;
+    const int tiles_r = (g.OH + TR - 1) / TR, tiles_c = (g.OW + TC - 1) / TC;
+    const int pitch = (TC + 4 + g.KW + 3 + 3) / 4 * 4 + 4;  // vector reads stay in the row
+    const size_t smem = (size_t)(TR + g.KH - 1) * pitch * sizeof(float);
+    const long long nblk = (long long)g.N * g.C * tiles_r * tiles_c;
+    const int threads = (TC / 4) * (TR / 4);
+#define FCONV_DW_BLOCK(KV)                                                                     \
+  if (g.KW == KV) {                                                                            \
+    auto k = dw_kernel_block<T, KV, KV>;                                                       \
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);          \
+    k<<<(unsigned)nblk, threads, smem, s>>>(g, x, w, b, z, y, TR, TC, tiles_r, tiles_c, pitch); \
+    return (int)cudaGetLastError();                                                            \
   }
-  FCONV_DW_FAST(3)
-  FCONV_DW_FAST(5)
-  FCONV_DW_FAST(7)
-#undef FCONV_DW_FAST
+    FCONV_DW_BLOCK(3)
+    FCONV_DW_BLOCK(5)
+    FCONV_DW_BLOCK(7)
+#undef FCONV_DW_BLOCK
+  }
   auto k = dw_kernel_generic<T>;
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem);
   k<<<(unsigned)blocks, kDwThreads, L.smem, s>>>(g, x, w, b, z, y, L.band, L.bands, L.srows,

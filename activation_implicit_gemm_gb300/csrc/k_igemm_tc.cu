@@ -61,12 +61,13 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kWarps = 14;
+constexpr int kWarps = 18;
 constexpr int kThreads = kWarps * 32;
-constexpr int kEpiWarp0 = 0;     // warps 0-3
-constexpr int kGatherWarp0 = 4;  // warps 4-11
-constexpr int kMmaWarp = 12;
-constexpr int kTmaWarp = 13;
+constexpr int kEpiWarp0 = 0;     // warps 0-7 (two per TMEM lane quarter)
+constexpr int kEpiWarps = 8;
+constexpr int kGatherWarp0 = 8;  // warps 8-15
+constexpr int kMmaWarp = 16;
+constexpr int kTmaWarp = 17;
 constexpr int kMaxStages = 8;
 constexpr int kMaxTab = 2048;    // tap (channel-inner) or k (generic) table entries
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -139,15 +140,18 @@ __device__ __forceinline__ void epi_store16(const float (&v)[16], const uint32_t
                                             const uint32_t (&br)[16], bool hz, bool hb,
                                             int nvalid, __half* yp, long long P, float alpha,
                                             float beta) {
+  // all 16 results first (independent chains), then the stores
+  __half h[16];
 #pragma unroll
   for (int jj = 0; jj < 16; ++jj) {
-    if (jj < nvalid) {
-      float t = v[jj];
-      if (hb) t += __half2float(__ushort_as_half((unsigned short)br[jj]));
-      if (hz) t += __half2float(__ushort_as_half((unsigned short)zr[jj]));
-      yp[(long long)jj * P] = __float2half_rn(act_eval<ACT, true>(t, alpha, beta));
-    }
+    float t = v[jj];
+    if (hb) t += __half2float(__ushort_as_half((unsigned short)br[jj]));
+    if (hz) t += __half2float(__ushort_as_half((unsigned short)zr[jj]));
+    h[jj] = __float2half_rn(act_eval<ACT, true>(t, alpha, beta));
   }
+#pragma unroll
+  for (int jj = 0; jj < 16; ++jj)
+    if (jj < nvalid) yp[(long long)jj * P] = h[jj];
 }
 
 // As epi_store16, but the 16 results go to this lane's column of the warp's staging tile
@@ -156,14 +160,17 @@ template <int ACT>
 __device__ __forceinline__ void epi_stage16(const float (&v)[16], const uint32_t (&zr)[16],
                                             const uint32_t (&br)[16], bool hz, bool hb,
                                             uint32_t col, float alpha, float beta) {
+  // all 16 results first (independent chains), then the shared-memory stores
+  uint32_t h[16];
 #pragma unroll
   for (int jj = 0; jj < 16; ++jj) {
     float t = v[jj];
     if (hb) t += __half2float(__ushort_as_half((unsigned short)br[jj]));
     if (hz) t += __half2float(__ushort_as_half((unsigned short)zr[jj]));
-    const __half h = __float2half_rn(act_eval<ACT, true>(t, alpha, beta));
-    ptx::st_shared_u16(col + jj * 64, __half_as_ushort(h));
+    h[jj] = __half_as_ushort(__float2half_rn(act_eval<ACT, true>(t, alpha, beta)));
   }
+#pragma unroll
+  for (int jj = 0; jj < 16; ++jj) ptx::st_shared_u16(col + jj * 64, h[jj]);
 }
 
 template <int BN, bool CHAN>
@@ -205,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(ptx::smem_addr(&ctl.acc_full[b]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl.acc_empty[b]), 4);  // 4 epilogue warps
+      ptx::mbar_init(ptx::smem_addr(&ctl.acc_empty[b]), kEpiWarps);
     }
     ptx::mbar_init(ptx::smem_addr(&ctl.drain), 1);
     ctl.abort_flag = 0;
@@ -385,9 +392,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       bounded_wait(ptx::smem_addr(&ctl.drain), 0, abort_flag);
     }
   } else {
-    // ================================================================ epilogue (warps 0-3)
-    const int r = (warp - kEpiWarp0) * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)((warp - kEpiWarp0) * 32) << 16);
+    // ================================================================ epilogue (warps 0-7)
+    const int q4 = (warp - kEpiWarp0) & 3;     // TMEM lane quarter
+    const int half = (warp - kEpiWarp0) >> 2;  // which alternate 16-column groups
+    const int r = q4 * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
     // 16-byte Y/Z vectors need 8-pixel groups inside one image (P % 8 == 0)
     const bool vec_io = (g.P % 8) == 0;
     const uint32_t yst = base + (uint32_t)S * kStageBytes + (uint32_t)(warp - kEpiWarp0) * 2048u;
@@ -408,12 +417,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int mc0 = un.ct * BN;
       // pixel group (8 consecutive pixels) this lane moves in the vector path
-      const long long gq = un.rt * kBM + (warp - kEpiWarp0) * 32 + (lane & 3) * 8;
+      const long long gq = un.rt * kBM + q4 * 32 + (lane & 3) * 8;
       const bool grp_ok = gq < NP;
       const long long gn = grp_ok ? gq / g.P : 0;
       const long long gp = grp_ok ? gq - gn * g.P : 0;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
+      for (int c0 = half * 16; c0 < BN; c0 += 32) {
         float v[16];
         __syncwarp();
         ptx::tmem_ld16(lane_base + b * kAccCols + (uint32_t)c0, v);
@@ -792,23 +801,36 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   }
 }
 
-// X (N, C, spatial S) -> Xb[c/64][n][s][64]: 64 x 64 tiles transposed through shared
-// memory, coalesced on both sides.
+// X (N, C, spatial S) -> Xb[c/64][n][s][64]. A block moves 64 channels x 128 pixels:
+// 16-byte loads along the pixels of each channel (8 pixels), a transpose through shared
+// memory, 16-byte stores of 8 channels of each pixel. Rows that are not 16-byte aligned
+// (S % 8 != 0) take 2-byte loads.
 __global__ void __launch_bounds__(256) pack_x_kernel(const uint16_t* __restrict__ x,
                                                      uint16_t* __restrict__ xb, int N, int C,
                                                      long long S) {
-  __shared__ uint16_t t[64][66];
-  const long long s0 = (long long)blockIdx.x * 64;
-  const int cb = blockIdx.y;
-  const int n = blockIdx.z;
+  __shared__ uint16_t t[64][128 + 8];
+  const long long s0 = (long long)blockIdx.x * 128;
+  const int cbn = blockIdx.y;  // cb * N + n
+  const int cb = cbn / N, n = cbn - cb * N;
   const uint16_t* src = x + ((long long)n * C + (long long)cb * 64) * S + s0;
-  for (int i = threadIdx.x; i < 64 * 64; i += 256) {
-    const int c = i >> 6, p = i & 63;
-    t[c][p] = (s0 + p < S) ? src[(long long)c * S + p] : (uint16_t)0;
+  const bool vec = (S % 8) == 0;
+  for (int i = threadIdx.x; i < 64 * 16; i += 256) {
+    const int c = i >> 4, p8 = (i & 15) * 8;
+    uint16_t e[8];
+    if (vec && s0 + p8 + 8 <= S) {
+      const uint4 v = *reinterpret_cast<const uint4*>(src + (long long)c * S + p8);
+      e[0] = (uint16_t)v.x; e[1] = (uint16_t)(v.x >> 16); e[2] = (uint16_t)v.y; e[3] = (uint16_t)(v.y >> 16);
+      e[4] = (uint16_t)v.z; e[5] = (uint16_t)(v.z >> 16); e[6] = (uint16_t)v.w; e[7] = (uint16_t)(v.w >> 16);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) e[k] = (s0 + p8 + k < S) ? src[(long long)c * S + p8 + k] : (uint16_t)0;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[c][p8 + k] = e[k];
   }
   __syncthreads();
-  uint16_t* dst = xb + (((long long)cb * N + n) * S + s0) * 64;
-  for (int j = threadIdx.x; j < 64 * 8; j += 256) {
+  uint16_t* dst = xb + ((long long)cbn * S + s0) * 64;
+  for (int j = threadIdx.x; j < 128 * 8; j += 256) {
     const int p = j >> 3, part = j & 7;
     if (s0 + p >= S) continue;
     uint32_t w[4];
@@ -820,30 +842,34 @@ __global__ void __launch_bounds__(256) pack_x_kernel(const uint16_t* __restrict_
 }
 
 // Weights in the GEMM's K order, zero padded to kpad columns: wp[m][k'] for k' < kpad.
+// One block per output channel; the row is staged in shared memory so the permuted
+// reads hit shared memory and both global sides are contiguous.
 __global__ void __launch_bounds__(256) prep_weights_kernel(const uint16_t* __restrict__ w,
                                                            uint16_t* __restrict__ wp, int M,
                                                            int Cg, int KV, int kpad, int chan) {
-  const long long total = (long long)M * kpad;
+  extern __shared__ uint16_t row[];
+  const int m = blockIdx.x;
   const int Kg = Cg * KV;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int m = (int)(i / kpad);
-    const int k = (int)(i - (long long)m * kpad);
+  const uint16_t* src = w + (long long)m * Kg;
+  for (int k = threadIdx.x; k < Kg; k += blockDim.x) row[k] = src[k];
+  __syncthreads();
+  uint16_t* dst = wp + (long long)m * kpad;
+  for (int k = threadIdx.x; k < kpad; k += blockDim.x) {
     uint16_t v = 0;
     if (k < Kg) {
-      int src = k;
+      int s = k;
       if (chan && (Cg % 64) == 0) {
         // (64-channel block, tap, channel)
         const int cb = k / (64 * KV), rem = k - cb * 64 * KV;
-        const int tap = rem / 64, ci = cb * 64 + (rem - tap * 64);
-        src = ci * KV + tap;
+        const int tap = rem >> 6, ci = cb * 64 + (rem & 63);
+        s = ci * KV + tap;
       } else if (chan) {
         const int tap = k / Cg, ci = k - tap * Cg;
-        src = ci * KV + tap;
+        s = ci * KV + tap;
       }
-      v = w[(long long)m * Kg + src];
+      v = row[s];
     }
-    wp[i] = v;
+    dst[k] = v;
   }
 }
 
@@ -899,7 +925,7 @@ struct TmaShape {
 TmaShape tma_shape(const ConvGeom& g) {
   TmaShape t{};
   t.ok = (g.Cg % kBK) == 0 && g.sD <= 8 && g.sH <= 8 && g.sW <= 8 &&
-         (long long)g.C * g.N <= 0x7fffffffLL / 64;
+         (long long)(g.C / 64) * g.N <= 65535;  // pack grid and the TMA box's last dim
   if (!t.ok) return t;
   t.Wt = min(g.OW, min(128, 256 / g.sW));
   t.Ht = min(g.OH, min(128 / t.Wt, 256 / g.sH));
@@ -1017,6 +1043,7 @@ long long igemm_tc_mtiles(const ConvGeom& g, int a_path) {
 bool igemm_tc_supported(const ConvGeom& g) {
   if (g.dtype != FCONV_F16) return false;
   if (g.KD > 32 || g.KH > 32 || g.KW > 32) return false;
+  if ((size_t)g.Kg * 2 > 200 * 1024) return false;  // weight row staged in shared memory
   if (channel_inner(g) ? g.KV > kMaxTab : g.Kg > kMaxTab) return false;
   // generic order: the per-k table holds ci * plane offsets in 32-bit ints
   if (!channel_inner(g) && (long long)g.Cg * g.IS > INT_MAX / 2) return false;
@@ -1039,11 +1066,15 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
   const int kpad = (int)kpad_of(g);
   if (pb) {
     uint16_t* wp = (uint16_t*)ws;
-    const long long total = (long long)g.M * kpad;
-    long long blocks = (total + 255) / 256;
-    if (blocks > 152LL * 16) blocks = 152LL * 16;
-    prep_weights_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)a.w, wp, g.M, g.Cg,
-                                                         g.KV, kpad, chan ? 1 : 0);
+    const size_t rowbytes = (size_t)g.Kg * 2;
+    if (rowbytes > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(prep_weights_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)rowbytes);
+      if (e != cudaSuccess) return (int)e;
+    }
+    prep_weights_kernel<<<(unsigned)g.M, 256, rowbytes, s>>>((const uint16_t*)a.w, wp, g.M, g.Cg,
+                                                             g.KV, kpad, chan ? 1 : 0);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
     wmat = wp;
@@ -1052,7 +1083,7 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
   const size_t xb_bytes = pack_bytes(g, c);
   if (tma) {
     const long long S = g.IS;
-    dim3 pg((unsigned)((S + 63) / 64), (unsigned)(g.C / 64), (unsigned)g.N);
+    dim3 pg((unsigned)((S + 127) / 128), (unsigned)((g.C / 64) * g.N), 1);
     pack_x_kernel<<<pg, 256, 0, s>>>((const uint16_t*)a.x, (uint16_t*)(ws + pb), g.N, g.C, S);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
