@@ -106,6 +106,9 @@ class FusedConvPlan:
         _check(lib.fconv_plan_work(self._ptr, ctypes.byref(fl), ctypes.byref(by)), "work")
         self.flops = fl.value
         self.bytes = by.value
+        nl = ctypes.c_int()
+        _check(lib.fconv_plan_launches(self._ptr, ctypes.byref(nl)), "launches")
+        self.launches = nl.value
         pb, pe = (ctypes.c_int64 * 3)(), (ctypes.c_int64 * 3)()
         _check(lib.fconv_plan_pads(self._ptr, pb, pe), "pads")
         self.pad_begin = tuple(pb)

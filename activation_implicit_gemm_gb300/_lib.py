@@ -44,6 +44,7 @@ class FconvOptions(ctypes.Structure):
 
 EXPORTS = ["fconv_plan_create", "fconv_plan_create_ex", "fconv_plan_output_shape",
            "fconv_plan_pads", "fconv_plan_workspace_size", "fconv_plan_route", "fconv_plan_work",
+           "fconv_plan_launches",
            "fconv_run", "fconv_check_device", "fconv_destroy", "fconv_status_string",
            "fconv_version"]
 
@@ -67,6 +68,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fconv_plan_workspace_size.argtypes = [vp, P(ctypes.c_size_t)]
     lib.fconv_plan_route.argtypes = [vp, P(ctypes.c_int), P(ctypes.c_int), P(ctypes.c_int)]
     lib.fconv_plan_work.argtypes = [vp, P(ctypes.c_double), P(ctypes.c_double)]
+    lib.fconv_plan_launches.argtypes = [vp, P(ctypes.c_int)]
     lib.fconv_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
     lib.fconv_check_device.argtypes = [vp]
     lib.fconv_destroy.argtypes = [vp]

@@ -298,6 +298,12 @@ fconv_status fconv_plan_route(const fconv_plan* p, fconv_route* route, int* tile
   return FCONV_OK;
 }
 
+fconv_status fconv_plan_launches(const fconv_plan* p, int* kernels) {
+  if (!p || !kernels) return FCONV_E_NULL;
+  *kernels = p->route == FCONV_ROUTE_IGEMM_TC ? igemm_tc_launches(p->g, p->igemm) : 1;
+  return FCONV_OK;
+}
+
 fconv_status fconv_plan_work(const fconv_plan* p, double* flops, double* bytes) {
   if (!p) return FCONV_E_NULL;
   const ConvGeom& g = p->g;

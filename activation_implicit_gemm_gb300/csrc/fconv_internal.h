@@ -58,6 +58,7 @@ size_t igemm_tc_smem_bytes(int tile_n, int stages);
 size_t igemm_tc_workspace_bytes(const ConvGeom& g, const IgemmConfig& c);
 long long igemm_tc_mtiles(const ConvGeom& g, int a_path);  // pixel tiles of the A operand
 bool igemm_tc_tma_capable(const ConvGeom& g);             // TMA-fed A path possible
+int igemm_tc_launches(const ConvGeom& g, const IgemmConfig& c);  // kernels per fconv_run
 
 // Device error word (set by kernels whose bounded waits gave up). Reads and clears.
 int read_and_clear_device_error(void* stream, unsigned* value);

@@ -161,16 +161,21 @@ __device__ __forceinline__ void epi_stage16(const float (&v)[16], const uint32_t
                                             const uint32_t (&br)[16], bool hz, bool hb,
                                             uint32_t col, float alpha, float beta) {
   // all 16 results first (independent chains), then the shared-memory stores
-  uint32_t h[16];
+  float o[16];
 #pragma unroll
   for (int jj = 0; jj < 16; ++jj) {
     float t = v[jj];
     if (hb) t += __half2float(__ushort_as_half((unsigned short)br[jj]));
     if (hz) t += __half2float(__ushort_as_half((unsigned short)zr[jj]));
-    h[jj] = __half_as_ushort(__float2half_rn(act_eval<ACT, true>(t, alpha, beta)));
+    o[jj] = act_eval<ACT, true>(t, alpha, beta);
   }
 #pragma unroll
-  for (int jj = 0; jj < 16; ++jj) ptx::st_shared_u16(col + jj * 64, h[jj]);
+  for (int jj = 0; jj < 16; jj += 2) {
+    // one packed conversion for two channels, then the two 2-byte stores
+    const __half2 h2 = __floats2half2_rn(o[jj], o[jj + 1]);
+    ptx::st_shared_u16(col + jj * 64, __half_as_ushort(__low2half(h2)));
+    ptx::st_shared_u16(col + (jj + 1) * 64, __half_as_ushort(__high2half(h2)));
+  }
 }
 
 template <int BN, bool CHAN>
@@ -801,49 +806,93 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   }
 }
 
-// X (N, C, spatial S) -> Xb[c/64][n][s][64]. A block moves 64 channels x 128 pixels:
-// 16-byte loads along the pixels of each channel (8 pixels), a transpose through shared
-// memory, 16-byte stores of 8 channels of each pixel. Rows that are not 16-byte aligned
-// (S % 8 != 0) take 2-byte loads.
+// X (N, C, spatial S) -> Xb[c/64][n][s][64]. Block (x, cb) moves 64 channels of the
+// flattened positions q = n*S + s in [128x, 128x + 128): four 16-byte loads per thread
+// (8 positions of one channel), all in flight, into a shared tile, then four 16-byte
+// stores per thread (8 channels of one position). Needs S % 8 == 0 (a load never
+// straddles two images); otherwise the scalar variant below is used.
 __global__ void __launch_bounds__(256) pack_x_kernel(const uint16_t* __restrict__ x,
                                                      uint16_t* __restrict__ xb, int N, int C,
                                                      long long S) {
-  __shared__ uint16_t t[64][128 + 8];
-  const long long s0 = (long long)blockIdx.x * 128;
-  const int cbn = blockIdx.y;  // cb * N + n
-  const int cb = cbn / N, n = cbn - cb * N;
-  const uint16_t* src = x + ((long long)n * C + (long long)cb * 64) * S + s0;
-  const bool vec = (S % 8) == 0;
-  for (int i = threadIdx.x; i < 64 * 16; i += 256) {
-    const int c = i >> 4, p8 = (i & 15) * 8;
-    uint16_t e[8];
-    if (vec && s0 + p8 + 8 <= S) {
-      const uint4 v = *reinterpret_cast<const uint4*>(src + (long long)c * S + p8);
-      e[0] = (uint16_t)v.x; e[1] = (uint16_t)(v.x >> 16); e[2] = (uint16_t)v.y; e[3] = (uint16_t)(v.y >> 16);
-      e[4] = (uint16_t)v.z; e[5] = (uint16_t)(v.z >> 16); e[6] = (uint16_t)v.w; e[7] = (uint16_t)(v.w >> 16);
-    } else {
+  constexpr int kPitch = 138;  // halves per channel row: 16-byte rows, few bank conflicts
+  __shared__ __align__(16) uint16_t t[64 * kPitch];
+  const long long NS = (long long)N * S;
+  const long long q0 = (long long)blockIdx.x * 128;
+  const int cb = blockIdx.y;
+  uint4 buf[4];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) e[k] = (s0 + p8 + k < S) ? src[(long long)c * S + p8 + k] : (uint16_t)0;
+  for (int i = 0; i < 4; ++i) {
+    const int v = threadIdx.x + 256 * i;
+    const int c = v >> 4, pv = v & 15;
+    const long long q = q0 + pv * 8;
+    buf[i] = make_uint4(0, 0, 0, 0);
+    if (q < NS) {
+      const long long n = q / S, sp = q - n * S;
+      buf[i] = *reinterpret_cast<const uint4*>(x + ((n * C + (long long)cb * 64 + c) * S + sp));
     }
+  }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) t[c][p8 + k] = e[k];
+  for (int i = 0; i < 4; ++i) {
+    const int v = threadIdx.x + 256 * i;
+    const int c = v >> 4, pv = v & 15;
+    uint32_t* d = reinterpret_cast<uint32_t*>(t + c * kPitch + pv * 8);  // 4-byte aligned
+    d[0] = buf[i].x; d[1] = buf[i].y; d[2] = buf[i].z; d[3] = buf[i].w;
   }
   __syncthreads();
-  uint16_t* dst = xb + ((long long)cbn * S + s0) * 64;
-  for (int j = threadIdx.x; j < 128 * 8; j += 256) {
-    const int p = j >> 3, part = j & 7;
-    if (s0 + p >= S) continue;
+  uint16_t* dst = xb + ((long long)cb * NS + q0) * 64;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int o = threadIdx.x + 256 * i;
+    const int p = o >> 3, part = o & 7;
+    if (q0 + p >= NS) continue;
     uint32_t w[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      w[e] = (uint32_t)t[8 * part + 2 * e][p] | ((uint32_t)t[8 * part + 2 * e + 1][p] << 16);
+      w[e] = (uint32_t)t[(8 * part + 2 * e) * kPitch + p] |
+             ((uint32_t)t[(8 * part + 2 * e + 1) * kPitch + p] << 16);
     *reinterpret_cast<uint4*>(dst + (long long)p * 64 + 8 * part) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
+// Scalar repack for S % 8 != 0: one thread per (position, 8 channels).
+__global__ void __launch_bounds__(256) pack_x_scalar_kernel(const uint16_t* __restrict__ x,
+                                                            uint16_t* __restrict__ xb, int N, int C,
+                                                            long long S) {
+  const long long NS = (long long)N * S;
+  const long long total = NS * (C / 8);
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += (long long)gridDim.x * 256) {
+    const long long q = i % NS;
+    const int c8 = (int)(i / NS);  // group of 8 channels
+    const long long n = q / S, sp = q - n * S;
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const long long c = (long long)c8 * 8 + 2 * e;
+      w[e] = (uint32_t)x[(n * C + c) * S + sp] | ((uint32_t)x[(n * C + c + 1) * S + sp] << 16);
+    }
+    const int cb = c8 / 8, part = c8 % 8;
+    *reinterpret_cast<uint4*>(xb + ((long long)cb * NS + q) * 64 + part * 8) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 // Weights in the GEMM's K order, zero padded to kpad columns: wp[m][k'] for k' < kpad.
-// One block per output channel; the row is staged in shared memory so the permuted
-// reads hit shared memory and both global sides are contiguous.
+// One block per output channel: the row is staged in shared memory (16-byte loads when
+// rows are 16-byte aligned), then each thread writes 8 consecutive k' as one 16-byte
+// store, reading the permuted sources from shared memory.
+__device__ __forceinline__ int prep_src(int k, int Cg, int KV, int chan) {
+  if (chan && (Cg % 64) == 0) {  // (64-channel block, tap, channel)
+    const int cb = k / (64 * KV), rem = k - cb * 64 * KV;
+    const int tap = rem >> 6;
+    return (cb * 64 + (rem & 63)) * KV + tap;
+  }
+  if (chan) {  // (tap, channel)
+    const int tap = k / Cg;
+    return (k - tap * Cg) * KV + tap;
+  }
+  return k;
+}
+
 __global__ void __launch_bounds__(256) prep_weights_kernel(const uint16_t* __restrict__ w,
                                                            uint16_t* __restrict__ wp, int M,
                                                            int Cg, int KV, int kpad, int chan) {
@@ -851,25 +900,23 @@ __global__ void __launch_bounds__(256) prep_weights_kernel(const uint16_t* __res
   const int m = blockIdx.x;
   const int Kg = Cg * KV;
   const uint16_t* src = w + (long long)m * Kg;
-  for (int k = threadIdx.x; k < Kg; k += blockDim.x) row[k] = src[k];
+  if ((Kg % 8) == 0) {
+    for (int v = threadIdx.x; v < Kg / 8; v += blockDim.x)
+      reinterpret_cast<uint4*>(row)[v] = reinterpret_cast<const uint4*>(src)[v];
+  } else {
+    for (int k = threadIdx.x; k < Kg; k += blockDim.x) row[k] = src[k];
+  }
   __syncthreads();
   uint16_t* dst = wp + (long long)m * kpad;
-  for (int k = threadIdx.x; k < kpad; k += blockDim.x) {
-    uint16_t v = 0;
-    if (k < Kg) {
-      int s = k;
-      if (chan && (Cg % 64) == 0) {
-        // (64-channel block, tap, channel)
-        const int cb = k / (64 * KV), rem = k - cb * 64 * KV;
-        const int tap = rem >> 6, ci = cb * 64 + (rem & 63);
-        s = ci * KV + tap;
-      } else if (chan) {
-        const int tap = k / Cg, ci = k - tap * Cg;
-        s = ci * KV + tap;
-      }
-      v = row[s];
+  for (int v = threadIdx.x; v < kpad / 8; v += blockDim.x) {
+    uint32_t e[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int k = v * 8 + j;
+      e[j] = k < Kg ? (uint32_t)row[prep_src(k, Cg, KV, chan)] : 0u;
     }
-    dst[k] = v;
+    reinterpret_cast<uint4*>(dst)[v] =
+        make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16), e[6] | (e[7] << 16));
   }
 }
 
@@ -925,7 +972,8 @@ struct TmaShape {
 TmaShape tma_shape(const ConvGeom& g) {
   TmaShape t{};
   t.ok = (g.Cg % kBK) == 0 && g.sD <= 8 && g.sH <= 8 && g.sW <= 8 &&
-         (long long)(g.C / 64) * g.N <= 65535;  // pack grid and the TMA box's last dim
+         (long long)(g.C / 64) * g.N <= 0x7fffffffLL &&  // the TMA box's last dim
+         (long long)g.N * g.IS / 128 < 0x7fffffffLL;     // pack grid
   if (!t.ok) return t;
   t.Wt = min(g.OW, min(128, 256 / g.sW));
   t.Ht = min(g.OH, min(128 / t.Wt, 256 / g.sH));
@@ -1035,6 +1083,10 @@ size_t igemm_tc_workspace_bytes(const ConvGeom& g, const IgemmConfig& c) {
 
 bool igemm_tc_tma_capable(const ConvGeom& g) { return tma_shape(g).ok; }
 
+int igemm_tc_launches(const ConvGeom& g, const IgemmConfig& c) {
+  return 1 + (needs_prep(g) ? 1 : 0) + (use_tma(g, c.a_path) ? 1 : 0) + (c.split_k > 1 ? 1 : 0);
+}
+
 long long igemm_tc_mtiles(const ConvGeom& g, int a_path) {
   if (use_tma(g, a_path)) return tma_shape(g).mtiles;
   return ((long long)g.N * g.P + kBM - 1) / kBM;
@@ -1083,8 +1135,16 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
   const size_t xb_bytes = pack_bytes(g, c);
   if (tma) {
     const long long S = g.IS;
-    dim3 pg((unsigned)((S + 127) / 128), (unsigned)((g.C / 64) * g.N), 1);
-    pack_x_kernel<<<pg, 256, 0, s>>>((const uint16_t*)a.x, (uint16_t*)(ws + pb), g.N, g.C, S);
+    const long long NS = (long long)g.N * S;
+    if (S % 8 == 0) {
+      dim3 pg((unsigned)((NS + 127) / 128), (unsigned)(g.C / 64), 1);
+      pack_x_kernel<<<pg, 256, 0, s>>>((const uint16_t*)a.x, (uint16_t*)(ws + pb), g.N, g.C, S);
+    } else {
+      long long blocks = (NS * (g.C / 8) + 255) / 256;
+      if (blocks > 152LL * 32) blocks = 152LL * 32;
+      pack_x_scalar_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)a.x,
+                                                             (uint16_t*)(ws + pb), g.N, g.C, S);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
   }

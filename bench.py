@@ -162,7 +162,7 @@ def run_ours(args):
                if plan.workspace_bytes else None)
         convs.append(dict(case=case, plan=plan, d=d, h=h, y=y, yh=yh, ws=wsb))
     total_flops = sum(c["plan"].flops for c in convs)
-    launches_per_step = sum(1 + (1 if c["plan"].split_k > 1 else 0) for c in convs)
+    launches_per_step = sum(c["plan"].launches for c in convs)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -316,13 +316,26 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def kernel_sources_digest():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "activation_implicit_gemm_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(conv_name):
-    """DRAM bytes per launch from a committed ncu summary, when one matches this conv."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes of one launch of this conv's main kernel from the committed ncu summary,
+    or None when there is none or the kernel sources changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    return d.get(conv_name)
+    if d.get("kernel_sources_sha256_16") != kernel_sources_digest():
+        return None
+    return d.get("per_launch_bytes", {}).get(conv_name)
 
 
 def cpu_baseline():

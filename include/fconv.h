@@ -168,6 +168,11 @@ fconv_status fconv_plan_workspace_size(const fconv_plan* plan, size_t* bytes);
 fconv_status fconv_plan_route(const fconv_plan* plan, fconv_route* route, int* tile_n,
                               int* split_k);
 
+/* Number of kernels one fconv_run of this plan launches (the convolution itself plus,
+ * on the tensor-core route, the weight reordering, the X repacking for the TMA-fed A
+ * operand and the split-K reduction, when the plan uses them). */
+fconv_status fconv_plan_launches(const fconv_plan* plan, int* kernels);
+
 /* Algorithmic work of one fconv_run: 2 * N * P * M * (C/group) * prod(kernel) flops and
  * the bytes of X, W, B, Z and Y each counted once. */
 fconv_status fconv_plan_work(const fconv_plan* plan, double* flops, double* bytes);
