@@ -16,6 +16,7 @@
 #include <cstring>
 #include <new>
 
+#include "fastdiv.cuh"
 #include "fconv_internal.h"
 
 using namespace fconv;
@@ -379,5 +380,28 @@ const char* fconv_status_string(fconv_status s) {
 }
 
 int fconv_version(void) { return 100; }
+
+// Host-side check of the invariant-divisor arithmetic the kernels use (a test hook, not
+// part of the documented ABI): 0 when every case agrees with ordinary division.
+int fconv_selftest_fastdiv(void) {
+  uint64_t state = 0x2545F4914F6CDD1Dull;
+  for (uint32_t d = 1; d < 5000; ++d) {
+    const FastDiv f = make_fastdiv(d);
+    for (int t = 0; t < 400; ++t) {
+      state ^= state << 13; state ^= state >> 7; state ^= state << 17;  // xorshift64
+      uint32_t n = (uint32_t)(state & 0x7fffffffu);
+      if (t < 8) n = (uint32_t)t * d + (uint32_t)(t & 1) * (d - 1);  // multiples and edges
+      if (t == 8) n = 0x7fffffffu;
+      if (fast_div(n, f) != n / d) return 1;
+    }
+  }
+  const uint32_t big[] = {65535u, 65536u, 100352u, 524288u, 3136u, 784u, 1u << 20, 0x7fffffffu};
+  for (uint32_t d : big) {
+    const FastDiv f = make_fastdiv(d);
+    for (uint32_t n : {0u, d - 1, d, 2 * d - 1, 0x7fffffffu, 0x7ffffffeu, 123456789u})
+      if (fast_div(n, f) != n / d) return 2;
+  }
+  return 0;
+}
 
 }  // extern "C"

@@ -50,6 +50,7 @@
 #include <mutex>
 
 #include "epilogue.cuh"
+#include "fastdiv.cuh"
 #include "fconv_internal.h"
 #include "ptx.cuh"
 
@@ -86,6 +87,7 @@ struct TcArgs {
   int ntiles;           // channel tiles per group
   long long row_tiles;  // ceil(N*P / 128)
   long long units;      // row_tiles * G * ntiles * split
+  FastDiv fd_split, fd_gnt, fd_P, fd_OW, fd_OH;  // unit and pixel decoding
 };
 
 struct SharedCtl {
@@ -123,12 +125,13 @@ struct Unit {
 
 __device__ __forceinline__ Unit decode_unit(long long u, const TcArgs& a, int G) {
   Unit t;
-  t.sp = (int)(u % a.split);
-  long long r = u / a.split;
-  const int gct = (int)(r % ((long long)G * a.ntiles));
-  t.rt = r / ((long long)G * a.ntiles);
-  t.grp = gct / a.ntiles;
-  t.ct = gct - t.grp * a.ntiles;
+  uint32_t r, sp, gct, rt;
+  fast_divmod((uint32_t)u, a.fd_split, r, sp);
+  fast_divmod(r, a.fd_gnt, rt, gct);
+  t.sp = (int)sp;
+  t.rt = rt;
+  t.grp = (int)gct / a.ntiles;
+  t.ct = (int)gct - t.grp * a.ntiles;
   t.c_begin = t.sp * a.chunks_per_split;
   t.nk = min(a.chunks_per_split, a.chunks - t.c_begin);
   return t;
@@ -247,11 +250,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = q < NP;
       int n = 0, od = 0, oh = 0, ow = 0;
       if (row_ok) {
-        n = (int)(q / g.P);
-        const long long o = q - (long long)n * g.P;
-        ow = (int)(o % g.OW);
-        oh = (int)((o / g.OW) % g.OH);
-        od = (int)(o / ((long long)g.OW * g.OH));
+        uint32_t nn, o, t1, w1, h1;
+        fast_divmod((uint32_t)q, a.fd_P, nn, o);
+        fast_divmod(o, a.fd_OW, t1, w1);
+        fast_divmod(t1, a.fd_OH, o, h1);
+        n = (int)nn; ow = (int)w1; oh = (int)h1; od = (int)o;
       }
       const int iz0 = od * g.sD - g.pD, iy0 = oh * g.sH - g.pH, ix0 = ow * g.sW - g.pW;
       uint32_t mz = 0, my = 0, mx = 0;  // bit t: tap t along that axis lands inside X
@@ -314,17 +317,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ci == g.Cg) { ci = 0; ++tap; }
           }
         } else {
-          // per-k table: the 64 table reads do not depend on each other or on the loads
+          // per-k table: the table reads do not depend on each other or on the loads;
+          // pieces of 8 past the end of K are skipped as a whole
 #pragma unroll
-          for (int e = 0; e < 64; ++e) {
-            uint32_t ok = 0;
-            const uint16_t* p = xg;
-            if (k0 + e < g.Kg) {
-              const int2 ti = tab[k0 + e];
-              ok = ((mz >> (ti.y & 0xff)) & (my >> ((ti.y >> 8) & 0xff)) & (mx >> (ti.y >> 16))) & 1u;
-              p = xg + ti.x;
+          for (int j = 0; j < 8; ++j) {
+            if (k0 + 8 * j < g.Kg) {
+#pragma unroll
+              for (int e = 8 * j; e < 8 * j + 8; ++e) {
+                uint32_t ok = 0;
+                const uint16_t* p = xg;
+                if (k0 + e < g.Kg) {
+                  const int2 ti = tab[k0 + e];
+                  ok = ((mz >> (ti.y & 0xff)) & (my >> ((ti.y >> 8) & 0xff)) & (mx >> (ti.y >> 16))) & 1u;
+                  p = xg + ti.x;
+                }
+                v[e] = ptx::ld1_u16(p, ok);
+              }
+            } else {
+#pragma unroll
+              for (int e = 8 * j; e < 8 * j + 8; ++e) v[e] = 0u;
             }
-            v[e] = ptx::ld1_u16(p, ok);
           }
         }
         const uint32_t arow = base + (uint32_t)s * kStageBytes + (uint32_t)r * 128u;
@@ -417,14 +429,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = q < NP;
       long long obase = 0;
       if (row_ok) {
-        const long long n = q / g.P;
+        const long long n = fast_div((uint32_t)q, a.fd_P);
         obase = n * g.M * g.P + (q - n * g.P);
       }
       const int mc0 = un.ct * BN;
       // pixel group (8 consecutive pixels) this lane moves in the vector path
       const long long gq = un.rt * kBM + q4 * 32 + (lane & 3) * 8;
       const bool grp_ok = gq < NP;
-      const long long gn = grp_ok ? gq / g.P : 0;
+      const long long gn = grp_ok ? (long long)fast_div((uint32_t)gq, a.fd_P) : 0;
       const long long gp = grp_ok ? gq - gn * g.P : 0;
 #pragma unroll 1
       for (int c0 = half * 16; c0 < BN; c0 += 32) {
@@ -547,6 +559,7 @@ struct TmaArgs {
   int vec;             // 8-row groups are 16-byte aligned, contiguous runs of Y
   uint32_t a_bytes;
   long long units;
+  FastDiv fd_split, fd_gnt, fd_nTw, fd_nTh, fd_nTd;
 };
 
 struct TmaUnit {
@@ -556,15 +569,15 @@ struct TmaUnit {
 
 __device__ __forceinline__ TmaUnit decode_tma_unit(long long u, const TmaArgs& a, int G) {
   TmaUnit t;
-  t.sp = (int)(u % a.split);
-  long long r = u / a.split;
-  const int gct = (int)(r % ((long long)G * a.ntiles));
-  long long rt = r / ((long long)G * a.ntiles);
-  t.grp = gct / a.ntiles;
-  t.ct = gct - t.grp * a.ntiles;
-  const int tw = (int)(rt % a.nTw); rt /= a.nTw;
-  const int th = (int)(rt % a.nTh); rt /= a.nTh;
-  const int td = (int)(rt % a.nTd); rt /= a.nTd;
+  uint32_t r, sp, gct, rt, tw, th, td;
+  fast_divmod((uint32_t)u, a.fd_split, r, sp);
+  fast_divmod(r, a.fd_gnt, rt, gct);
+  t.sp = (int)sp;
+  t.grp = (int)gct / a.ntiles;
+  t.ct = (int)gct - t.grp * a.ntiles;
+  fast_divmod(rt, a.fd_nTw, rt, tw);
+  fast_divmod(rt, a.fd_nTh, rt, th);
+  fast_divmod(rt, a.fd_nTd, rt, td);
   t.n0 = (int)rt * a.Nb;
   t.od0 = td * a.Dt;
   t.oh0 = th * a.Ht;
@@ -1096,6 +1109,8 @@ bool igemm_tc_supported(const ConvGeom& g) {
   if (g.dtype != FCONV_F16) return false;
   if (g.KD > 32 || g.KH > 32 || g.KW > 32) return false;
   if ((size_t)g.Kg * 2 > 200 * 1024) return false;  // weight row staged in shared memory
+  // unit and pixel indices are decoded in 32 bits (every unit count is at most N*P*M)
+  if ((long long)g.N * g.P * g.M >= 0x7fffffffLL) return false;
   if (channel_inner(g) ? g.KV > kMaxTab : g.Kg > kMaxTab) return false;
   // generic order: the per-k table holds ci * plane offsets in 32-bit ints
   if (!channel_inner(g) && (long long)g.Cg * g.IS > INT_MAX / 2) return false;
@@ -1195,6 +1210,11 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
     t.vec = sh.vec;
     t.a_bytes = (uint32_t)sh.rows * 128u;
     t.units = sh.mtiles * g.G * t.ntiles * c.split_k;
+    t.fd_split = make_fastdiv((uint32_t)c.split_k);
+    t.fd_gnt = make_fastdiv((uint32_t)(g.G * t.ntiles));
+    t.fd_nTw = make_fastdiv((uint32_t)t.nTw);
+    t.fd_nTh = make_fastdiv((uint32_t)t.nTh);
+    t.fd_nTd = make_fastdiv((uint32_t)t.nTd);
     int err;
     switch (c.tile_n) {
       case 16: err = launch_tma_t<16>(g, c, t, tx, tm, s); break;
@@ -1221,6 +1241,11 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
   ta.ntiles = (g.Mg + c.tile_n - 1) / c.tile_n;
   ta.row_tiles = ((long long)g.N * g.P + kBM - 1) / kBM;
   ta.units = ta.row_tiles * g.G * ta.ntiles * c.split_k;
+  ta.fd_split = make_fastdiv((uint32_t)c.split_k);
+  ta.fd_gnt = make_fastdiv((uint32_t)(g.G * ta.ntiles));
+  ta.fd_P = make_fastdiv((uint32_t)g.P);
+  ta.fd_OW = make_fastdiv((uint32_t)g.OW);
+  ta.fd_OH = make_fastdiv((uint32_t)g.OH);
   const int err = chan ? launch_bn<true>(g, c, ta, tm, s) : launch_bn<false>(g, c, ta, tm, s);
   if (err != 0 || c.split_k <= 1) return err;
   return launch_reduce(g, c, part, ta.b, ta.z, ta.y, s);

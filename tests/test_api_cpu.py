@@ -224,3 +224,9 @@ def test_status_strings(lib):
     for code in _lib.STATUS:
         assert lib.fconv_status_string(code)
     assert lib.fconv_version() >= 100
+
+
+def test_invariant_divisor_arithmetic(lib):
+    """The multiply-shift division the kernels use for index decoding agrees with
+    ordinary integer division (checked by the library's host code)."""
+    assert lib.fconv_selftest_fastdiv() == 0
