@@ -210,6 +210,112 @@ __global__ void __launch_bounds__(256) dw_kernel_block(ConvGeom g, const T* __re
 #undef FCONV_DW_STORE
 }
 
+
+// Persistent variant for planes that fit one tile (OH <= 64, OW <= 64) with stride 1,
+// dilation 1: a CTA loops over (image, channel) planes. The zero padding of the fp32
+// tile is written once (every plane has the same halo), the next plane's input rows are
+// loaded into registers while the current plane is computed, and each thread's Z values
+// are requested before its FMA loop so their latency hides behind it.
+template <typename T, int KH, int KW, int MAXV>
+__global__ void __launch_bounds__(256) dw_kernel_persistent(ConvGeom g, const T* __restrict__ x,
+                                                            const T* __restrict__ w,
+                                                            const T* __restrict__ b,
+                                                            const T* __restrict__ z,
+                                                            T* __restrict__ y, int TR, int TC,
+                                                            int pitch, long long planes) {
+  extern __shared__ float sx[];
+  constexpr int WIN = 4 + KW - 1;
+  constexpr int WV = (WIN + 3) / 4;
+  constexpr int VE = 16 / sizeof(T);
+  // rows of the tile: the last block row of threads reads up to row TR + KH - 2 (TR is OH
+  // rounded up to a multiple of 4)
+  const int srows = TR + KH - 1;
+  const int ixb = -g.pW - 4;                 // input column of tile column 0
+  const int nvr = g.IW / VE;                 // 16-byte vectors per input row
+  const int nvec = g.IH * nvr;               // per plane
+  for (int i = threadIdx.x * 4; i < srows * pitch; i += blockDim.x * 4)
+    *reinterpret_cast<float4*>(sx + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int tcols = TC / 4;
+  const int ty = threadIdx.x / tcols, tx = threadIdx.x - ty * tcols;
+  const int oy = ty * 4, ox = tx * 4;
+  const bool active = oy < g.OH && ox < g.OW;
+  const int nv = active ? min(4, g.OW - ox) : 0, nr = active ? min(4, g.OH - oy) : 0;
+
+  uint4 pre[MAXV];
+  auto prefetch = [&](long long plane) {
+    const T* xp = x + plane * g.IS;
+#pragma unroll
+    for (int u = 0; u < MAXV; ++u) {
+      const int i = threadIdx.x + u * blockDim.x;
+      if (i < nvec) pre[u] = *reinterpret_cast<const uint4*>(xp + (long long)i * VE);
+    }
+  };
+  long long plane = blockIdx.x;
+  if (plane < planes) prefetch(plane);
+  for (; plane < planes; plane += gridDim.x) {
+    const int c = (int)(plane % g.C);
+    float wr[KH * KW];
+#pragma unroll
+    for (int i = 0; i < KH * KW; ++i) wr[i] = to_f32(w[(long long)c * KH * KW + i]);
+    const float bias = b ? to_f32(b[c]) : 0.0f;
+    __syncthreads();  // the previous plane's compute is done with the tile
+#pragma unroll
+    for (int u = 0; u < MAXV; ++u) {
+      const int i = threadIdx.x + u * blockDim.x;
+      if (i < nvec) {
+        const int iy = i / nvr, c0 = (i - iy * nvr) * VE;
+        const T* e = reinterpret_cast<const T*>(&pre[u]);
+        float* d = sx + (iy + g.pH) * pitch + (c0 - ixb);
+#pragma unroll
+        for (int k = 0; k < VE; ++k) d[k] = to_f32(e[k]);
+      }
+    }
+    __syncthreads();
+    const long long next = plane + gridDim.x;
+    if (next < planes) prefetch(next);
+    const long long obase = plane * g.P + (long long)oy * g.OW + ox;
+    float zv[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        zv[r][j] = (z && r < nr && j < nv) ? to_f32(z[obase + (long long)r * g.OW + j]) : 0.0f;
+    if (active) {
+      float acc[4][4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[r][j] = bias + zv[r][j];
+      const float* base = sx + oy * pitch + ox + 4;
+#pragma unroll
+      for (int ir = 0; ir < 4 + KH - 1; ++ir) {
+        float win[WV * 4];
+        const float4* rp = reinterpret_cast<const float4*>(base + ir * pitch);
+#pragma unroll
+        for (int q = 0; q < WV; ++q) {
+          const float4 f = rp[q];
+          win[4 * q] = f.x; win[4 * q + 1] = f.y; win[4 * q + 2] = f.z; win[4 * q + 3] = f.w;
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int ky = ir - r;
+          if (ky < 0 || ky >= KH) continue;
+#pragma unroll
+          for (int kx = 0; kx < KW; ++kx) {
+            const float wv = wr[ky * KW + kx];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[r][j] = fmaf(win[j + kx], wv, acc[r][j]);
+          }
+        }
+      }
+      // Z is already in the accumulators
+#define FCONV_DW_STORE(ACT) store_block4<ACT, T>(acc, (const T*)nullptr, y, obase, g.OW, nr, nv, g.alpha, g.beta)
+      FCONV_ACT_SWITCH(g.act, FCONV_DW_STORE)
+#undef FCONV_DW_STORE
+    }
+  }
+}
+
 // General path: any stride and dilation, one output per thread iteration.
 template <typename T>
 __global__ void __launch_bounds__(kDwThreads) dw_kernel_generic(ConvGeom g, const T* __restrict__ x,
@@ -259,6 +365,37 @@ int launch_dw_t(const ConvGeom& g, const ConvArgs& a, cudaStream_t s) {
   const T* z = (const T*)a.z;
   T* y = (T*)a.y;
   const bool unit = g.sW == 1 && g.dW == 1 && g.sH == 1 && g.dH == 1;
+  constexpr int VE = 16 / sizeof(T);
+  if (unit && g.KH == g.KW && (g.KW == 3 || g.KW == 5 || g.KW == 7) && g.OH <= 64 &&
+      g.OW <= 64 && g.IW % VE == 0 && g.IS % VE == 0 &&
+      (long long)g.IH * (g.IW / VE) <= 4LL * ((g.OW + 3) / 4) * ((g.OH + 3) / 4) &&
+      g.IH + g.pH <= g.OH + g.KH - 1 && g.IW + g.pW + 4 <= (g.OW + 3) / 4 * 4 + 4 + g.KW + 3) {
+    // persistent CTAs; the whole plane is one tile
+    const int TC = (g.OW + 3) / 4 * 4;
+    const int TR = (g.OH + 3) / 4 * 4;
+    const int threads = (TC / 4) * (TR / 4);
+    const int pitch = (TC + 4 + g.KW + 3 + 3) / 4 * 4 + 4;
+    const size_t smem = (size_t)(TR + g.KH - 1) * pitch * sizeof(float);
+    const long long planes = (long long)g.N * g.C;
+    int dev = 0, sms = 152;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+#define FCONV_DW_PERSIST(KV)                                                                    \
+  if (g.KW == KV) {                                                                             \
+    auto k = dw_kernel_persistent<T, KV, KV, 4>;                                                \
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);           \
+    int per_sm = 1;                                                                             \
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem);                  \
+    long long grid = (long long)sms * (per_sm > 0 ? per_sm : 1);                                \
+    if (grid > planes) grid = planes;                                                           \
+    k<<<(unsigned)grid, threads, smem, s>>>(g, x, w, b, z, y, TR, TC, pitch, planes);           \
+    return (int)cudaGetLastError();                                                             \
+  }
+    FCONV_DW_PERSIST(3)
+    FCONV_DW_PERSIST(5)
+    FCONV_DW_PERSIST(7)
+#undef FCONV_DW_PERSIST
+  }
   if (unit && g.KH == g.KW && (g.KW == 3 || g.KW == 5 || g.KW == 7)) {
     // output tile: TC columns (<= 64, a multiple of 4), TR rows, at most 256 threads
     const int TC = min(64, (g.OW + 3) / 4 * 4);

@@ -200,6 +200,9 @@ DW_CASES = [
     ((1, 8, 16, 19), 3, dict(dilations=[2, 3], pads=[2, 0, 1, 3])),
     ((1, 4, 9, 9), 4, dict(pads=[1, 2, 2, 1])),
     ((2, 3, 200, 220), 3, dict(pads=[1, 1, 1, 1])),  # several row bands per plane
+    ((3, 16, 24, 32), 3, dict(pads=[1, 1, 1, 1])),    # persistent: one tile per plane
+    ((2, 8, 56, 56), 7, dict(pads=[3, 3, 3, 3])),     # persistent, the stem's geometry
+    ((2, 4, 8, 8), 5, dict(pads=[2, 2, 2, 2])),
 ]
 
 
