@@ -724,19 +724,35 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       if (*abort_flag) break;
       const TmaUnit un = decode_tma_unit(u, a, g.G);
       const uint32_t b = tcount & 1u;
+      const int gn = un.n0 + gnb, god = un.od0 + gdt, goh = un.oh0 + ght, gow = un.ow0 + gwt;
+      const bool grp_ok =
+          gr < a.rows && gn < g.N && god < g.OD && goh < g.OH && gow < g.OW;
+      const long long gpix = ((long long)god * g.OH + goh) * g.OW + gow;
+      const int mc0 = un.ct * BN;
+      // Z vectors of the next 16-column group, requested one group ahead (the first one
+      // before waiting for the accumulator) so the load latency overlaps other work
+      const bool zvec = a.vec && a.z != nullptr && a.part == nullptr;
+      uint4 zn0 = make_uint4(0, 0, 0, 0), zn1 = make_uint4(0, 0, 0, 0);
+      auto load_z = [&](int c0, uint4& z0, uint4& z1) {
+        const int mcb = mc0 + c0;
+        const long long zb = ((long long)gn * g.M + un.grp * g.Mg + mcb) * g.P + gpix;
+        const int ch0 = lane >> 2, ch1 = (lane >> 2) + 8;
+        z0 = (grp_ok && c0 < BN && mcb + ch0 < g.Mg) ? ptx::ldg_nc_v4(a.z + zb + (long long)ch0 * g.P)
+                                                    : make_uint4(0, 0, 0, 0);
+        z1 = (grp_ok && c0 < BN && mcb + ch1 < g.Mg) ? ptx::ldg_nc_v4(a.z + zb + (long long)ch1 * g.P)
+                                                    : make_uint4(0, 0, 0, 0);
+      };
+      if (zvec) load_z(half * 16, zn0, zn1);
       if (!bounded_wait(ptx::smem_addr(&ctl.acc_full[b]), (tcount >> 1) & 1, abort_flag)) break;
       ptx::tc_fence_after();
       const int n = un.n0 + nb, od = un.od0 + dt, oh = un.oh0 + ht, ow = un.ow0 + wt;
       const bool row_ok = r < a.rows && n < g.N && od < g.OD && oh < g.OH && ow < g.OW;
       const long long obase =
           row_ok ? (long long)n * g.M * g.P + ((long long)od * g.OH + oh) * g.OW + ow : 0;
-      const int gn = un.n0 + gnb, god = un.od0 + gdt, goh = un.oh0 + ght, gow = un.ow0 + gwt;
-      const bool grp_ok =
-          gr < a.rows && gn < g.N && god < g.OD && goh < g.OH && gow < g.OW;
-      const long long gpix = ((long long)god * g.OH + goh) * g.OW + gow;
-      const int mc0 = un.ct * BN;
 #pragma unroll 1
       for (int c0 = half * 16; c0 < BN; c0 += 32) {
+        const uint4 zc0 = zn0, zc1 = zn1;
+        if (zvec && c0 + 32 < BN) load_z(c0 + 32, zn0, zn1);
         float v[16];
         __syncwarp();
         ptx::tmem_ld16(lane_base + b * kAccCols + (uint32_t)c0, v);
@@ -756,14 +772,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         }
         if (a.vec) {
           if (hz) {
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              const int ch = (lane >> 2) + 8 * t;
-              uint4 zv = make_uint4(0, 0, 0, 0);
-              if (grp_ok && ch < nvalid)
-                zv = ptx::ldg_nc_v4(a.z + (((long long)gn * g.M + m0 + ch) * g.P + gpix));
-              ptx::st_shared_v4(zst + ch * 64 + (lane & 3) * 16, zv.x, zv.y, zv.z, zv.w);
-            }
+            ptx::st_shared_v4(zst + (lane >> 2) * 64 + (lane & 3) * 16, zc0.x, zc0.y, zc0.z, zc0.w);
+            ptx::st_shared_v4(zst + ((lane >> 2) + 8) * 64 + (lane & 3) * 16, zc1.x, zc1.y, zc1.z,
+                              zc1.w);
             __syncwarp();
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) zr[jj] = ptx::ld_shared_u16(zst + jj * 64 + lane * 2);
