@@ -15,6 +15,14 @@
 
 namespace fconv {
 
+// First tap t with i0 + t*d >= 0, and one past the last tap with i0 + t*d < n (k taps).
+__device__ __forceinline__ int tap_lo(int i0, int d) { return i0 >= 0 ? 0 : (-i0 + d - 1) / d; }
+__device__ __forceinline__ int tap_hi(int i0, int d, int n, int k) {
+  if (i0 >= n) return 0;
+  const int h = (n - i0 + d - 1) / d;
+  return h < k ? h : k;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) direct_conv_kernel(ConvGeom g, const T* __restrict__ x,
                                                           const T* __restrict__ w,
@@ -32,23 +40,22 @@ __global__ void __launch_bounds__(256) direct_conv_kernel(ConvGeom g, const T* _
     const int od = (int)(o / ((long long)g.OW * g.OH));
     const int grp = m / g.Mg;
     const int iz0 = od * g.sD - g.pD, iy0 = oh * g.sH - g.pH, ix0 = ow * g.sW - g.pW;
+    // the taps that land inside X, per axis (no test in the inner loops)
+    const int z0 = tap_lo(iz0, g.dD), z1 = tap_hi(iz0, g.dD, g.ID, g.KD);
+    const int y0 = tap_lo(iy0, g.dH), y1 = tap_hi(iy0, g.dH, g.IH, g.KH);
+    const int x0 = tap_lo(ix0, g.dW), x1 = tap_hi(ix0, g.dW, g.IW, g.KW);
     float acc = 0.0f;
     for (int ci = 0; ci < g.Cg; ++ci) {
       const T* xp = x + ((long long)n * g.C + (long long)grp * g.Cg + ci) * g.IS;
       const T* wp = w + ((long long)m * g.Cg + ci) * g.KV;
-      for (int kz = 0; kz < g.KD; ++kz) {
+      for (int kz = z0; kz < z1; ++kz) {
         const int iz = iz0 + kz * g.dD;
-        if (iz < 0 || iz >= g.ID) continue;
-        for (int ky = 0; ky < g.KH; ++ky) {
+        for (int ky = y0; ky < y1; ++ky) {
           const int iy = iy0 + ky * g.dH;
-          if (iy < 0 || iy >= g.IH) continue;
-          const T* xrow = xp + ((long long)iz * g.IH + iy) * g.IW;
+          const T* xrow = xp + ((long long)iz * g.IH + iy) * g.IW + ix0;
           const T* wrow = wp + (kz * g.KH + ky) * g.KW;
-          for (int kx = 0; kx < g.KW; ++kx) {
-            const int ix = ix0 + kx * g.dW;
-            if (ix < 0 || ix >= g.IW) continue;
-            acc = fmaf(to_f32(xrow[ix]), to_f32(wrow[kx]), acc);
-          }
+#pragma unroll 4
+          for (int kx = x0; kx < x1; ++kx) acc = fmaf(to_f32(xrow[kx * g.dW]), to_f32(wrow[kx]), acc);
         }
       }
     }

@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ SharedCtl ctl;
   // channel-inner: per tap {offset in the X plane, kz | ky << 8 | kx << 16};
   // generic: per k {offset from the group's first channel plane, same tap bits}
-  __shared__ int2 tab[kMaxTab];
+  __shared__ __align__(16) int2 tab[kMaxTab];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -206,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int HW = g.IH * g.IW;
 
   const int ntab = CHAN ? g.KV : g.Kg;
+  for (int t = ntab + tid; t < ((ntab + 7) & ~7) && t < kMaxTab; t += kThreads) tab[t] = make_int2(0, 0);
   for (int t = tid; t < ntab && t < kMaxTab; t += kThreads) {
     const int ci = CHAN ? 0 : t / g.KV;
     const int tap = CHAN ? t : t - ci * g.KV;
@@ -322,16 +323,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             if (k0 + 8 * j < g.Kg) {
+              // the piece's 8 table entries first (broadcast reads, independent), then its
+              // 8 loads back to back; the table is padded past Kg so the reads stay in it
+              int2 te[8];
+              const int4* tp = reinterpret_cast<const int4*>(&tab[k0 + 8 * j]);
 #pragma unroll
-              for (int e = 8 * j; e < 8 * j + 8; ++e) {
-                uint32_t ok = 0;
-                const uint16_t* p = xg;
-                if (k0 + e < g.Kg) {
-                  const int2 ti = tab[k0 + e];
-                  ok = ((mz >> (ti.y & 0xff)) & (my >> ((ti.y >> 8) & 0xff)) & (mx >> (ti.y >> 16))) & 1u;
-                  p = xg + ti.x;
-                }
-                v[e] = ptx::ld1_u16(p, ok);
+              for (int h = 0; h < 4; ++h) {
+                const int4 t4 = tp[h];
+                te[2 * h] = make_int2(t4.x, t4.y);
+                te[2 * h + 1] = make_int2(t4.z, t4.w);
+              }
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int2 ti = te[e];
+                const uint32_t ok =
+                    (k0 + 8 * j + e < g.Kg) &&
+                    (((mz >> (ti.y & 0xff)) & (my >> ((ti.y >> 8) & 0xff)) & (mx >> (ti.y >> 16))) & 1u);
+                v[8 * j + e] = ptx::ld1_u16(xg + ti.x, ok);
               }
             } else {
 #pragma unroll
