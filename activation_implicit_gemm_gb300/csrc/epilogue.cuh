@@ -56,6 +56,37 @@ __device__ __forceinline__ float sigmoid_fast(float t) {
   return fmaf(0.5f, th, 0.5f);
 }
 
+// Hardware approximations (PTX rcp.approx / ex2.approx): relative error a few ulp of f32.
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// Exact (erf) GELU, x * Phi(x), with Phi(x) = 1 - erfc(x / sqrt 2) / 2 for x >= 0 and
+// erfc(|x| / sqrt 2) / 2 for x < 0. erfc(z) for z >= 0 is Hastings' rational
+// approximation as tabulated in Abramowitz & Stegun, Handbook of Mathematical Functions,
+// formula 7.1.26: t = 1 / (1 + p z), erfc(z) = (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5)
+// exp(-z^2), |error| <= 1.5e-7. With the approximate reciprocal and exponential the
+// error of Phi stays below 3e-7 absolute, far below an f16 rounding of x * Phi(x).
+// Used only for f16 outputs.
+__device__ __forceinline__ float gelu_erf_fast(float x) {
+  const float z = fabsf(x) * 0.70710678118654752f;
+  const float t = rcp_approx(fmaf(0.3275911f, z, 1.0f));
+  float p = fmaf(1.061405429f, t, -1.453152027f);
+  p = fmaf(p, t, 1.421413741f);
+  p = fmaf(p, t, -0.284496736f);
+  p = fmaf(p, t, 0.254829592f);
+  const float q = p * t * ex2_approx(-1.4426950408889634f * z * z);  // erfc(z)
+  const float phi = x >= 0.0f ? fmaf(-0.5f, q, 1.0f) : 0.5f * q;
+  return x * phi;
+}
+
 template <int ACT, bool FAST>
 __device__ __forceinline__ float act_eval(float v, float alpha, float beta) {
   if constexpr (ACT == FCONV_ACT_NONE) {
@@ -80,7 +111,7 @@ __device__ __forceinline__ float act_eval(float v, float alpha, float beta) {
     return v > 0.0f ? v : alpha * (FAST ? (__expf(v) - 1.0f) : expm1f(v));
   } else if constexpr (ACT == FCONV_ACT_GELU) {
     if (alpha != 0.0f) return gelu_tanh_f(v);
-    return 0.5f * v * (1.0f + erff(v * 0.7071067811865476f));
+    return FAST ? gelu_erf_fast(v) : 0.5f * v * (1.0f + erff(v * 0.7071067811865476f));
   } else if constexpr (ACT == FCONV_ACT_FASTGELU) {
     return gelu_tanh_f(v);
   } else if constexpr (ACT == FCONV_ACT_SOFTPLUS) {

@@ -182,7 +182,7 @@ void plan_igemm(fconv_plan* p, const fconv_options* o) {
   c.a_path = o ? o->a_path : 0;
   const long long rows = igemm_tc_mtiles(g, c.a_path);
   const long long tiles = rows * ((g.Mg + c.tile_n - 1) / c.tile_n) * g.G;
-  const int chunks = (g.Kg + 63) / 64;
+  const int chunks = igemm_tc_chunks(g, c.a_path);
   int split = 1;
   if (o && o->split_k > 0) {
     split = o->split_k;
@@ -233,7 +233,8 @@ fconv_status create(const fconv_desc* d, int device, const fconv_options* o, fco
     st = FCONV_E_UNSUPPORTED;
   }
   if (st == FCONV_OK && route == FCONV_ROUTE_IGEMM_TC && o &&
-      (o->a_path < 0 || o->a_path > 2 || (o->a_path == 2 && !igemm_tc_tma_capable(p->g))))
+      (o->a_path < 0 || o->a_path > 2 || (o->a_path == 2 && !igemm_tc_tma_capable(p->g)) ||
+       (o->a_path == 1 && !igemm_tc_gather_capable(p->g))))
     st = FCONV_E_UNSUPPORTED;
   if (st == FCONV_OK && route == FCONV_ROUTE_IGEMM_TC && o && o->tile_n &&
       (o->tile_n < 16 || o->tile_n > 256 || (o->tile_n & (o->tile_n - 1)) != 0))

@@ -57,7 +57,9 @@ int igemm_tc_stages(int tile_n);
 size_t igemm_tc_smem_bytes(int tile_n, int stages);
 size_t igemm_tc_workspace_bytes(const ConvGeom& g, const IgemmConfig& c);
 long long igemm_tc_mtiles(const ConvGeom& g, int a_path);  // pixel tiles of the A operand
+int igemm_tc_chunks(const ConvGeom& g, int a_path);        // 64-wide K chunks of the GEMM
 bool igemm_tc_tma_capable(const ConvGeom& g);             // TMA-fed A path possible
+bool igemm_tc_gather_capable(const ConvGeom& g);          // gathered A path possible
 int igemm_tc_launches(const ConvGeom& g, const IgemmConfig& c);  // kernels per fconv_run
 
 // Device error word (set by kernels whose bounded waits gave up). Reads and clears.

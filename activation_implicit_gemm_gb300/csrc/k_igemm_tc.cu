@@ -70,24 +70,39 @@ constexpr int kGatherWarp0 = 8;  // warps 8-15
 constexpr int kMmaWarp = 16;
 constexpr int kTmaWarp = 17;
 constexpr int kMaxStages = 8;
-constexpr int kMaxTab = 2048;    // tap (channel-inner) or k (generic) table entries
+constexpr int kMaxTab = 2048;    // per-piece table entries (16-byte pieces of a GEMM row)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Shared-memory ring depth for a tile width: as many (A 16 KB + B) chunks as fit in
+// 200 KB, at most kMaxStages, even (the two gather sets alternate chunks).
+__host__ __device__ constexpr int stages_for(int bn) {
+  const int st = (200 * 1024) / (kBM * kBK * 2 + bn * kBK * 2);
+  const int capped = (st > kMaxStages ? kMaxStages : st) & ~1;
+  return capped < 2 ? 2 : capped;
+}
+// Chunks whose copies a gather thread keeps in flight. Each set then holds at most
+// depth - 1 chunks that are loaded but not yet handed to the MMA while it waits for a free
+// stage, and the stage it waits for was consumed after chunks older than all of those:
+// with stages >= 2 * depth the wait never depends on an arrival still owed by a gather set.
+__host__ __device__ constexpr int gather_depth(int bn) { return stages_for(bn) / 2 < 4 ? stages_for(bn) / 2 : 4; }
 constexpr unsigned kErrWaitTimeout = 1u;
 
 struct TcArgs {
-  const uint16_t* x;
+  const uint16_t* xc;   // X repacked channels-last: [G][N][pixel][cp]
   const __half* b;
   const __half* z;
   __half* y;
   float* part;          // split-K partials [split][N][M][P] (f32), or null
   int stages;
-  int chunks;           // ceil(Kg / 64)
+  int cp, cp8;          // channels per packed pixel (C/group rounded up to 8), cp / 8
+  int npieces;          // KV * cp8: 16-byte pieces of a GEMM row
+  int chunks;           // ceil(KV * cp / 64)
   int chunks_per_split;
   int split;
   int ntiles;           // channel tiles per group
   long long row_tiles;  // ceil(N*P / 128)
   long long units;      // row_tiles * G * ntiles * split
-  FastDiv fd_split, fd_gnt, fd_P, fd_OW, fd_OH;  // unit and pixel decoding
+  FastDiv fd_split, fd_gnt, fd_ntiles, fd_P, fd_OW, fd_OH;  // unit and pixel decoding
 };
 
 struct SharedCtl {
@@ -130,48 +145,48 @@ __device__ __forceinline__ Unit decode_unit(long long u, const TcArgs& a, int G)
   fast_divmod(r, a.fd_gnt, rt, gct);
   t.sp = (int)sp;
   t.rt = rt;
-  t.grp = (int)gct / a.ntiles;
+  t.grp = (int)fast_div(gct, a.fd_ntiles);
   t.ct = (int)gct - t.grp * a.ntiles;
   t.c_begin = t.sp * a.chunks_per_split;
   t.nk = min(a.chunks_per_split, a.chunks - t.c_begin);
   return t;
 }
 
-// Bias, residual, activation and f16 rounding for the (up to) 16 channels of one pixel.
-template <int ACT>
-__device__ __forceinline__ void epi_store16(const float (&v)[16], const uint32_t (&zr)[16],
-                                            const uint32_t (&br)[16], bool hz, bool hb,
-                                            int nvalid, __half* yp, long long P, float alpha,
-                                            float beta) {
-  // all 16 results first (independent chains), then the stores
-  __half h[16];
-#pragma unroll
-  for (int jj = 0; jj < 16; ++jj) {
-    float t = v[jj];
-    if (hb) t += __half2float(__ushort_as_half((unsigned short)br[jj]));
-    if (hz) t += __half2float(__ushort_as_half((unsigned short)zr[jj]));
-    h[jj] = __float2half_rn(act_eval<ACT, true>(t, alpha, beta));
-  }
-#pragma unroll
-  for (int jj = 0; jj < 16; ++jj)
-    if (jj < nvalid) yp[(long long)jj * P] = h[jj];
+// ---------------------------------------------------------------- epilogue
+// TMEM lane = output pixel, column = output channel. A warp owns one 32-lane quarter and
+// every other 16-column group of the accumulator; per group it loads 16 f32 columns,
+// adds B[m] and Z, applies the activation, rounds to f16 and stores NC(D)HW Y. In the
+// vector path (P % 8 == 0) the 16 x 32 results go through the warp's staging tile
+// [16 channels][32 pixels] so that Z and Y move as 16-byte vectors (8 pixels of one
+// channel); otherwise each lane stores its own pixel's 16 channels.
+
+// Where one tile's rows land in Y: this lane's pixel, and the 8-pixel group this lane
+// moves in the vector path (lane l: pixels 8 (l % 4) .. 8 (l % 4) + 7 of its quarter).
+struct EpiRows {
+  bool row_ok;      // this lane's pixel exists
+  long long obase;  // n * M * P + pixel index of this lane's pixel
+  bool grp_ok;      // this lane's 8-pixel group exists
+  long long gbase;  // n * M * P + first pixel of that group
+};
+
+// Z of channels mcb + lane / 4 and mcb + lane / 4 + 8 for this lane's pixel group.
+__device__ __forceinline__ void load_z16(const __half* z, const EpiRows& er, int mcb, int m_end,
+                                         long long P, int lane, uint4& z0, uint4& z1) {
+  const int ch0 = lane >> 2, ch1 = ch0 + 8;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  z0 = (er.grp_ok && mcb + ch0 < m_end) ? ptx::ldg_nc_v4(z + er.gbase + (long long)(mcb + ch0) * P)
+                                        : zero;
+  z1 = (er.grp_ok && mcb + ch1 < m_end) ? ptx::ldg_nc_v4(z + er.gbase + (long long)(mcb + ch1) * P)
+                                        : zero;
 }
 
-// As epi_store16, but the 16 results go to this lane's column of the warp's staging tile
-// (channel-major, 64 bytes per channel row) for the vector store.
+// Activation of 16 pre-activation values and f16 rounding into this lane's column of the
+// staging tile (64 bytes per channel row).
 template <int ACT>
-__device__ __forceinline__ void epi_stage16(const float (&v)[16], const uint32_t (&zr)[16],
-                                            const uint32_t (&br)[16], bool hz, bool hb,
-                                            uint32_t col, float alpha, float beta) {
-  // all 16 results first (independent chains), then the shared-memory stores
+__device__ __forceinline__ void stage16(const float (&v)[16], uint32_t col, float alpha, float beta) {
   float o[16];
 #pragma unroll
-  for (int jj = 0; jj < 16; ++jj) {
-    float t = v[jj];
-    if (hb) t += __half2float(__ushort_as_half((unsigned short)br[jj]));
-    if (hz) t += __half2float(__ushort_as_half((unsigned short)zr[jj]));
-    o[jj] = act_eval<ACT, true>(t, alpha, beta);
-  }
+  for (int jj = 0; jj < 16; ++jj) o[jj] = act_eval<ACT, true>(v[jj], alpha, beta);
 #pragma unroll
   for (int jj = 0; jj < 16; jj += 2) {
     // one packed conversion for two channels, then the two 2-byte stores
@@ -181,7 +196,134 @@ __device__ __forceinline__ void epi_stage16(const float (&v)[16], const uint32_t
   }
 }
 
-template <int BN, bool CHAN>
+// One tile's epilogue for this warp. acc = TMEM address of the warp's lane quarter in the
+// tile's accumulator buffer; channels [m_first, m_first + BN) of the tile, of which those
+// below m_end exist; part = split-K partials of this unit's split (raw sums, nothing else
+// applied) or null; zn0/zn1 = Z of the warp's first group, already requested.
+template <int BN, int ACT>
+__device__ __forceinline__ void epilogue_tile(const ConvGeom& g, const __half* b, const __half* z,
+                                              __half* y, float* part, bool vec,
+                                              const EpiRows& er, int m_first, int m_end,
+                                              uint32_t acc, int half, int lane, uint32_t yst,
+                                              uint32_t zst, uint4 zn0, uint4 zn1) {
+  const bool hz = z != nullptr, hb = b != nullptr;
+#pragma unroll 1
+  for (int c0 = half * 16; c0 < BN; c0 += 32) {
+    const int mcb = m_first + c0;
+    if (mcb >= m_end) break;  // the same for the whole warp
+    const int nvalid = min(16, m_end - mcb);
+    const uint4 zc0 = zn0, zc1 = zn1;
+    if (vec && hz && c0 + 32 < BN) load_z16(z, er, mcb + 32, m_end, g.P, lane, zn0, zn1);
+    uint32_t bl = 0;  // bias of channel mcb + lane % 16, requested before the accumulator
+    if (hb && !part) bl = ptx::ld1_u16(b + mcb + (lane & 15), (lane & 15) < nvalid ? 1u : 0u);
+    float v[16];
+    __syncwarp();
+    ptx::tmem_ld16(acc + (uint32_t)c0, v);
+    if (part) {
+      if (er.row_ok) {
+        float* pp = part + er.obase + (long long)mcb * g.P;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj)
+          if (jj < nvalid) pp[(long long)jj * g.P] = v[jj];
+      }
+      continue;
+    }
+    if (hb) {
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj)
+        v[jj] += __half2float(__ushort_as_half((unsigned short)__shfl_sync(0xffffffffu, bl, jj)));
+    }
+    if (vec) {
+      if (hz) {
+        ptx::st_shared_v4(zst + (lane >> 2) * 64 + (lane & 3) * 16, zc0.x, zc0.y, zc0.z, zc0.w);
+        ptx::st_shared_v4(zst + ((lane >> 2) + 8) * 64 + (lane & 3) * 16, zc1.x, zc1.y, zc1.z, zc1.w);
+        __syncwarp();
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj)
+          v[jj] += __half2float(__ushort_as_half((unsigned short)ptx::ld_shared_u16(zst + jj * 64 + lane * 2)));
+      }
+      stage16<ACT>(v, yst + lane * 2, g.alpha, g.beta);
+      __syncwarp();
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int ch = (lane >> 2) + 8 * t;
+        if (er.grp_ok && ch < nvalid) {
+          const uint4 yv = ptx::ld_shared_v4(yst + ch * 64 + (lane & 3) * 16);
+          ptx::st_global_v4(y + er.gbase + (long long)(mcb + ch) * g.P, yv);
+        }
+      }
+      __syncwarp();
+      continue;
+    }
+    if (!er.row_ok) continue;
+    const long long yb = er.obase + (long long)mcb * g.P;
+    if (hz) {
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj)
+        v[jj] += __half2float(__ushort_as_half(
+            (unsigned short)ptx::ld1_u16(z + yb + (long long)jj * g.P, jj < nvalid ? 1u : 0u)));
+    }
+    __half h[16];
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) h[jj] = __float2half_rn(act_eval<ACT, true>(v[jj], g.alpha, g.beta));
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj)
+      if (jj < nvalid) y[yb + (long long)jj * g.P] = h[jj];
+  }
+}
+
+// Epilogue warps of the gathered-A kernel: tile rows are 128 consecutive output pixels
+// q = n * P + pixel.
+template <int BN, int ACT>
+__device__ __forceinline__ void gather_epilogue(const ConvGeom& g, const TcArgs& a, SharedCtl& ctl,
+                                                uint32_t tmem, uint32_t staging, int warp, int lane) {
+  constexpr uint32_t kAccCols = BN < 32 ? 32 : BN;
+  const int q4 = (warp - kEpiWarp0) & 3;     // TMEM lane quarter
+  const int half = (warp - kEpiWarp0) >> 2;  // which alternate 16-column groups
+  const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+  // 16-byte Y/Z vectors need 8-pixel groups inside one image (P % 8 == 0)
+  const bool vec = (g.P % 8) == 0;
+  const uint32_t yst = staging + (uint32_t)(warp - kEpiWarp0) * 2048u;
+  const uint32_t zst = yst + 1024u;
+  const long long NP = (long long)g.N * g.P;
+  const long long MP = (long long)g.M * g.P;
+  volatile int* abort_flag = &ctl.abort_flag;
+  uint32_t tcount = 0;
+  for (long long u = blockIdx.x; u < a.units; u += gridDim.x, ++tcount) {
+    if (*abort_flag) break;
+    const Unit un = decode_unit(u, a, g.G);
+    const uint32_t b = tcount & 1u;
+    EpiRows er;
+    const long long q = un.rt * kBM + q4 * 32 + lane;
+    er.row_ok = q < NP;
+    er.obase = 0;
+    if (er.row_ok) {
+      const long long n = fast_div((uint32_t)q, a.fd_P);
+      er.obase = n * MP + (q - n * g.P);
+    }
+    const long long gq = un.rt * kBM + q4 * 32 + (lane & 3) * 8;
+    er.grp_ok = gq < NP;
+    er.gbase = 0;
+    if (er.grp_ok) {
+      const long long gn = fast_div((uint32_t)gq, a.fd_P);
+      er.gbase = gn * MP + (gq - gn * g.P);
+    }
+    const int m_first = un.grp * g.Mg + un.ct * BN, m_end = un.grp * g.Mg + g.Mg;
+    float* part = a.part ? a.part + (long long)un.sp * NP * g.M : nullptr;
+    uint4 zn0 = make_uint4(0, 0, 0, 0), zn1 = zn0;
+    if (vec && a.z && !part && m_first + half * 16 < m_end)
+      load_z16(a.z, er, m_first + half * 16, m_end, g.P, lane, zn0, zn1);
+    if (!bounded_wait(ptx::smem_addr(&ctl.acc_full[b]), (tcount >> 1) & 1, abort_flag)) break;
+    ptx::tc_fence_after();
+    epilogue_tile<BN, ACT>(g, a.b, a.z, a.y, part, vec, er, m_first, m_end, lane_base + b * kAccCols,
+                           half, lane, yst, zst, zn0, zn1);
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl.acc_empty[b]));
+  }
+}
+
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     igemm_tc_kernel(const ConvGeom g, const TcArgs a, const __grid_constant__ CUtensorMap tmap_w) {
   constexpr uint32_t kAccCols = BN < 32 ? 32 : BN;
@@ -193,8 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   extern __shared__ uint8_t dsmem[];
   __shared__ SharedCtl ctl;
-  // channel-inner: per tap {offset in the X plane, kz | ky << 8 | kx << 16};
-  // generic: per k {offset from the group's first channel plane, same tap bits}
+  // per 16-byte piece p of a GEMM row (tap p / cp8, channels 8 (p % cp8) ..): {offset from
+  // the row's first packed pixel in elements, (ky * KW + kx) | kz << 8}; pieces past the
+  // end of K carry kz = 31, a bit that no row's depth mask has
   __shared__ __align__(16) int2 tab[kMaxTab];
 
   const int tid = threadIdx.x;
@@ -205,14 +348,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long NP = (long long)g.N * g.P;
   const int HW = g.IH * g.IW;
 
-  const int ntab = CHAN ? g.KV : g.Kg;
-  for (int t = ntab + tid; t < ((ntab + 7) & ~7) && t < kMaxTab; t += kThreads) tab[t] = make_int2(0, 0);
-  for (int t = tid; t < ntab && t < kMaxTab; t += kThreads) {
-    const int ci = CHAN ? 0 : t / g.KV;
-    const int tap = CHAN ? t : t - ci * g.KV;
-    const int kx = tap % g.KW, ky = (tap / g.KW) % g.KH, kz = tap / (g.KW * g.KH);
-    tab[t] = make_int2(ci * (int)g.IS + kz * g.dD * HW + ky * g.dH * g.IW + kx * g.dW,
-                       kz | (ky << 8) | (kx << 16));
+  for (int p = tid; p < a.chunks * 8 && p < kMaxTab; p += kThreads) {
+    if (p < a.npieces) {
+      const int t = p / a.cp8, c8 = p - t * a.cp8;
+      const int kx = t % g.KW, ky = (t / g.KW) % g.KH, kz = t / (g.KW * g.KH);
+      tab[p] = make_int2((kz * g.dD * HW + ky * g.dH * g.IW + kx * g.dW) * a.cp + c8 * 8,
+                         (ky * g.KW + kx) | (kz << 8));
+    } else {
+      tab[p] = make_int2(0, 31 << 8);
+    }
   }
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -243,7 +387,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int set = (warp - kGatherWarp0) >> 2;
     const int r = ((warp - kGatherWarp0) & 3) * 32 + lane;  // tile row
     const uint32_t swz = (uint32_t)(r & 7);
-    uint32_t it = 0;
+    constexpr int kDepth = gather_depth(BN);
+    uint32_t it = 0, last_it = 0;
+    int pending = 0;  // chunks of this set whose copies are in flight, newest = last_it
     for (long long u = blockIdx.x; u < a.units; u += gridDim.x) {
       if (*abort_flag) break;
       const Unit un = decode_unit(u, a, g.G);
@@ -258,102 +404,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         n = (int)nn; ow = (int)w1; oh = (int)h1; od = (int)o;
       }
       const int iz0 = od * g.sD - g.pD, iy0 = oh * g.sH - g.pH, ix0 = ow * g.sW - g.pW;
-      uint32_t mz = 0, my = 0, mx = 0;  // bit t: tap t along that axis lands inside X
+      // bit kz of mz: depth tap kz lands inside X; bit ky * KW + kx of mhw: the (ky, kx)
+      // tap does (KH * KW <= 64)
+      uint32_t mz = 0, mx = 0;
+      uint64_t mhw = 0;
       for (int t = 0; t < g.KD; ++t) { const int v = iz0 + t * g.dD; if (v >= 0 && v < g.ID) mz |= 1u << t; }
-      for (int t = 0; t < g.KH; ++t) { const int v = iy0 + t * g.dH; if (v >= 0 && v < g.IH) my |= 1u << t; }
       for (int t = 0; t < g.KW; ++t) { const int v = ix0 + t * g.dW; if (v >= 0 && v < g.IW) mx |= 1u << t; }
+      for (int t = 0; t < g.KH; ++t) {
+        const int v = iy0 + t * g.dH;
+        if (v >= 0 && v < g.IH) mhw |= (uint64_t)mx << (t * g.KW);
+      }
       if (!row_ok) mz = 0;
-      const uint16_t* xg = a.x + ((long long)n * g.C + (long long)un.grp * g.Cg) * g.IS +
-                           ((iz0 * g.IH + iy0) * g.IW + ix0);
+      // this row's first packed pixel (possibly outside X: only valid taps are read)
+      const uint16_t* xg =
+          a.xc + ((long long)(un.grp * g.N + n) * g.IS + ((iz0 * g.IH + iy0) * g.IW + ix0)) * a.cp;
       for (int i = 0; i < un.nk; ++i, ++it) {
         if ((int)(it & 1u) != set) continue;
         const int s = (int)(it % (uint32_t)S);
         if (it >= (uint32_t)S &&
             !bounded_wait(ptx::smem_addr(&ctl.empty[s]), ((it / S) - 1) & 1, abort_flag))
           break;
-        const int k0 = (un.c_begin + i) * kBK;
-        uint32_t v[64];
-        if (CHAN && (g.Cg % kBK) == 0) {
-          // K order (64-channel block, tap, channel): the chunk is 64 channels of one tap,
-          // and the taps of a block follow each other, so the block's slab of X stays in
-          // L1 across them. One validity test, 64 loads one channel plane apart, all in
-          // flight before any store.
-          const int chunk = un.c_begin + i;
-          const int cb = chunk / g.KV;
-          const int tap = chunk - cb * g.KV;
-          const int ci = cb * kBK;
-          const int2 ti = tab[tap];
-          const bool ok = ((mz >> (ti.y & 0xff)) & (my >> ((ti.y >> 8) & 0xff)) & (mx >> (ti.y >> 16))) & 1u;
-          if (ok) {
-            const uint16_t* p = xg + (long long)ci * g.IS + ti.x;
+        // the chunk's eight 16-byte pieces: one validity test and one asynchronous 16-byte
+        // copy each, straight into the 128-byte-swizzled row (zero fill for taps outside X,
+        // pieces past K and rows past N*P)
+        const int4* tp = reinterpret_cast<const int4*>(&tab[(un.c_begin + i) * 8]);
+        const uint32_t arow = (base + (uint32_t)s * kStageBytes + (uint32_t)r * 128u) | (swz << 4);
 #pragma unroll
-            for (int e = 0; e < 64; ++e) v[e] = __ldg(p + (long long)e * g.IS);
-          } else {
+        for (int h = 0; h < 4; ++h) {
+          const int4 t2 = tp[h];
 #pragma unroll
-            for (int e = 0; e < 64; ++e) v[e] = 0u;
-          }
-        } else if (CHAN) {
-          // eight pieces of 8 channels; each piece is one tap: one validity test, eight
-          // loads one channel plane apart, all 64 loads in flight before any store
-          int tap = k0 / g.Cg;
-          int ci = k0 - tap * g.Cg;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int kk = k0 + 8 * j;
-            uint32_t ok = 0;
-            const uint16_t* p = xg;
-            if (kk < g.Kg) {
-              const int2 ti = tab[tap];
-              ok = ((mz >> (ti.y & 0xff)) & (my >> ((ti.y >> 8) & 0xff)) & (mx >> (ti.y >> 16))) & 1u;
-              p = xg + (long long)ci * g.IS + ti.x;
-            }
-            uint32_t(&v8)[8] = *reinterpret_cast<uint32_t(*)[8]>(&v[8 * j]);
-            if (ok) {
-              ptx::ld8_u16_nz(v8, p, g.IS * 2);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) v8[e] = 0u;
-            }
-            ci += 8;
-            if (ci == g.Cg) { ci = 0; ++tap; }
-          }
-        } else {
-          // per-k table: the table reads do not depend on each other or on the loads;
-          // pieces of 8 past the end of K are skipped as a whole
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (k0 + 8 * j < g.Kg) {
-              // the piece's 8 table entries first (broadcast reads, independent), then its
-              // 8 loads back to back; the table is padded past Kg so the reads stay in it
-              int2 te[8];
-              const int4* tp = reinterpret_cast<const int4*>(&tab[k0 + 8 * j]);
-#pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                const int4 t4 = tp[h];
-                te[2 * h] = make_int2(t4.x, t4.y);
-                te[2 * h + 1] = make_int2(t4.z, t4.w);
-              }
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const int2 ti = te[e];
-                const uint32_t ok =
-                    (k0 + 8 * j + e < g.Kg) &&
-                    (((mz >> (ti.y & 0xff)) & (my >> ((ti.y >> 8) & 0xff)) & (mx >> (ti.y >> 16))) & 1u);
-                v[8 * j + e] = ptx::ld1_u16(xg + ti.x, ok);
-              }
-            } else {
-#pragma unroll
-              for (int e = 8 * j; e < 8 * j + 8; ++e) v[e] = 0u;
-            }
+          for (int e = 0; e < 2; ++e) {
+            const int off = e ? t2.z : t2.x, bits = e ? t2.w : t2.y;
+            const uint32_t ok = (uint32_t)(mhw >> (bits & 0xff)) & (mz >> (bits >> 8)) & 1u;
+            ptx::cp_async16(arow ^ ((uint32_t)(2 * h + e) << 4), ok ? xg + off : a.xc, ok ? 16u : 0u);
           }
         }
-        const uint32_t arow = base + (uint32_t)s * kStageBytes + (uint32_t)r * 128u;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) ptx::st_shared_pack8(arow + (((uint32_t)j ^ swz) << 4), &v[8 * j]);
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl.full[s]));
+        ptx::cp_async_commit();
+        last_it = it;
+        if (++pending == kDepth) {
+          // the oldest chunk in flight (kDepth - 1 chunks of this set ago) has landed
+          ptx::cp_async_wait<kDepth - 1>();
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          const uint32_t old = it - 2u * (kDepth - 1);
+          if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl.full[old % (uint32_t)S]));
+          --pending;
+        }
       }
+    }
+    // hand over the chunks still in flight (also after an abort: copies always complete)
+    ptx::cp_async_wait<0>();
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    for (int k = pending - 1; k >= 0; --k) {
+      const uint32_t old = last_it - 2u * (uint32_t)k;
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl.full[old % (uint32_t)S]));
     }
   } else if (warp == kTmaWarp) {
     // ================================================================ weights by TMA
@@ -418,112 +523,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ================================================================ epilogue (warps 0-7)
-    const int q4 = (warp - kEpiWarp0) & 3;     // TMEM lane quarter
-    const int half = (warp - kEpiWarp0) >> 2;  // which alternate 16-column groups
-    const int r = q4 * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
-    // 16-byte Y/Z vectors need 8-pixel groups inside one image (P % 8 == 0)
-    const bool vec_io = (g.P % 8) == 0;
-    const uint32_t yst = base + (uint32_t)S * kStageBytes + (uint32_t)(warp - kEpiWarp0) * 2048u;
-    const uint32_t zst = yst + 1024u;
-    uint32_t tcount = 0;
-    for (long long u = blockIdx.x; u < a.units; u += gridDim.x, ++tcount) {
-      if (*abort_flag) break;
-      const Unit un = decode_unit(u, a, g.G);
-      const uint32_t b = tcount & 1u;
-      if (!bounded_wait(ptx::smem_addr(&ctl.acc_full[b]), (tcount >> 1) & 1, abort_flag)) break;
-      ptx::tc_fence_after();
-      const long long q = un.rt * kBM + r;
-      const bool row_ok = q < NP;
-      long long obase = 0;
-      if (row_ok) {
-        const long long n = fast_div((uint32_t)q, a.fd_P);
-        obase = n * g.M * g.P + (q - n * g.P);
-      }
-      const int mc0 = un.ct * BN;
-      // pixel group (8 consecutive pixels) this lane moves in the vector path
-      const long long gq = un.rt * kBM + q4 * 32 + (lane & 3) * 8;
-      const bool grp_ok = gq < NP;
-      const long long gn = grp_ok ? (long long)fast_div((uint32_t)gq, a.fd_P) : 0;
-      const long long gp = grp_ok ? gq - gn * g.P : 0;
-#pragma unroll 1
-      for (int c0 = half * 16; c0 < BN; c0 += 32) {
-        float v[16];
-        __syncwarp();
-        ptx::tmem_ld16(lane_base + b * kAccCols + (uint32_t)c0, v);
-        // the vector path needs every lane (shuffles, warp syncs); invalid rows there are
-        // whole 8-pixel groups that are never stored
-        if (!row_ok && !(vec_io && a.part == nullptr)) continue;
-        const int mcb = mc0 + c0;
-        const int nvalid = min(16, g.Mg - mcb);
-        if (nvalid <= 0) continue;
-        const long long yb = obase + (long long)(un.grp * g.Mg + mcb) * g.P;
-        if (a.part) {
-          float* pp = a.part + (long long)un.sp * NP * g.M + yb;
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj)
-            if (jj < nvalid) pp[(long long)jj * g.P] = v[jj];
-          continue;
-        }
-        const bool hz = a.z != nullptr, hb = a.b != nullptr;
-        uint32_t zr[16], br[16];
-        if (vec_io) {
-          // Z and Y move as 16-byte vectors (8 pixels of one channel) through this warp's
-          // staging tile [16 channels][32 pixels]; lane l owns pixel group l % 4 and
-          // channels l / 4 and l / 4 + 8 for the vector moves
-          const int m0 = un.grp * g.Mg + mcb;
-          if (hz) {
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              const int ch = (lane >> 2) + 8 * t;
-              uint4 zv = make_uint4(0, 0, 0, 0);
-              if (grp_ok && ch < nvalid)
-                zv = ptx::ldg_nc_v4(a.z + ((gn * g.M + m0 + ch) * g.P + gp));
-              ptx::st_shared_v4(zst + ch * 64 + (lane & 3) * 16, zv.x, zv.y, zv.z, zv.w);
-            }
-            __syncwarp();
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) zr[jj] = ptx::ld_shared_u16(zst + jj * 64 + lane * 2);
-          }
-          if (hb) {
-            const uint32_t bl = ptx::ld1_u16(a.b + m0 + (lane & 15), (lane & 15) < nvalid ? 1u : 0u);
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) br[jj] = __shfl_sync(0xffffffffu, bl, jj);
-          }
-#define FCONV_EPI16S(ACT) epi_stage16<ACT>(v, zr, br, hz, hb, yst + lane * 2, g.alpha, g.beta)
-          FCONV_ACT_SWITCH(g.act, FCONV_EPI16S)
-#undef FCONV_EPI16S
-          __syncwarp();
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const int ch = (lane >> 2) + 8 * t;
-            if (grp_ok && ch < nvalid) {
-              const uint4 yv = ptx::ld_shared_v4(yst + ch * 64 + (lane & 3) * 16);
-              ptx::st_global_v4(a.y + ((gn * g.M + m0 + ch) * g.P + gp), yv);
-            }
-          }
-          __syncwarp();
-          continue;
-        }
-        if (hz) {
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj)
-            zr[jj] = ptx::ld1_u16(a.z + yb + (long long)jj * g.P, jj < nvalid ? 1u : 0u);
-        }
-        if (hb) {
-          const __half* bp = a.b + un.grp * g.Mg + mcb;
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) br[jj] = ptx::ld1_u16(bp + jj, jj < nvalid ? 1u : 0u);
-        }
-        __half* yp = a.y + yb;
-#define FCONV_EPI16(ACT) epi_store16<ACT>(v, zr, br, hz, hb, nvalid, yp, g.P, g.alpha, g.beta)
-        FCONV_ACT_SWITCH(g.act, FCONV_EPI16)
-#undef FCONV_EPI16
-      }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl.acc_empty[b]));
-    }
+    // one loop per activation, chosen once: the group loop carries no dispatch
+#define FCONV_EPI_LOOP(ACT) gather_epilogue<BN, ACT>(g, a, ctl, tmem, base + (uint32_t)S * kStageBytes, warp, lane)
+    FCONV_ACT_SWITCH(g.act, FCONV_EPI_LOOP)
+#undef FCONV_EPI_LOOP
   }
 
   ptx::tc_fence_before();
@@ -567,7 +570,7 @@ struct TmaArgs {
   int vec;             // 8-row groups are 16-byte aligned, contiguous runs of Y
   uint32_t a_bytes;
   long long units;
-  FastDiv fd_split, fd_gnt, fd_nTw, fd_nTh, fd_nTd;
+  FastDiv fd_split, fd_gnt, fd_ntiles, fd_nTw, fd_nTh, fd_nTd;
 };
 
 struct TmaUnit {
@@ -581,7 +584,7 @@ __device__ __forceinline__ TmaUnit decode_tma_unit(long long u, const TmaArgs& a
   fast_divmod((uint32_t)u, a.fd_split, r, sp);
   fast_divmod(r, a.fd_gnt, rt, gct);
   t.sp = (int)sp;
-  t.grp = (int)gct / a.ntiles;
+  t.grp = (int)fast_div(gct, a.fd_ntiles);
   t.ct = (int)gct - t.grp * a.ntiles;
   fast_divmod(rt, a.fd_nTw, rt, tw);
   fast_divmod(rt, a.fd_nTh, rt, th);
@@ -593,6 +596,55 @@ __device__ __forceinline__ TmaUnit decode_tma_unit(long long u, const TmaArgs& a
   t.c_begin = t.sp * a.chunks_per_split;
   t.nk = min(a.chunks_per_split, a.chunks - t.c_begin);
   return t;
+}
+
+// Epilogue warps of the TMA-fed kernel: tile rows are the pixels of a box (Nb images x
+// Dt x Ht x Wt), row r = ((nb * Dt + dt) * Ht + ht) * Wt + wt.
+template <int BN, int ACT>
+__device__ __forceinline__ void tma_epilogue(const ConvGeom& g, const TmaArgs& a, SharedCtl& ctl,
+                                             uint32_t tmem, uint32_t staging, int warp, int lane) {
+  constexpr uint32_t kAccCols = BN < 32 ? 32 : BN;
+  const int q = warp & 3;      // TMEM lane quarter
+  const int half = warp >> 2;  // which alternate 16-column groups
+  const int r = q * 32 + lane;
+  const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+  const uint32_t yst = staging + (uint32_t)warp * 2048u;
+  const uint32_t zst = yst + 1024u;
+  // this row's place in the pixel box, and that of the 8-row group this lane moves
+  const int wt = r % a.Wt, ht = (r / a.Wt) % a.Ht, dt = (r / (a.Wt * a.Ht)) % a.Dt;
+  const int nb = r / (a.Wt * a.Ht * a.Dt);
+  const int gr = q * 32 + (lane & 3) * 8;
+  const int gwt = gr % a.Wt, ght = (gr / a.Wt) % a.Ht, gdt = (gr / (a.Wt * a.Ht)) % a.Dt;
+  const int gnb = gr / (a.Wt * a.Ht * a.Dt);
+  const long long NP = (long long)g.N * g.P;
+  const long long MP = (long long)g.M * g.P;
+  const bool vec = a.vec != 0;
+  volatile int* abort_flag = &ctl.abort_flag;
+  uint32_t tcount = 0;
+  for (long long u = blockIdx.x; u < a.units; u += gridDim.x, ++tcount) {
+    if (*abort_flag) break;
+    const TmaUnit un = decode_tma_unit(u, a, g.G);
+    const uint32_t b = tcount & 1u;
+    EpiRows er;
+    const int n = un.n0 + nb, od = un.od0 + dt, oh = un.oh0 + ht, ow = un.ow0 + wt;
+    er.row_ok = r < a.rows && n < g.N && od < g.OD && oh < g.OH && ow < g.OW;
+    er.obase = er.row_ok ? (long long)n * MP + ((long long)od * g.OH + oh) * g.OW + ow : 0;
+    const int gn = un.n0 + gnb, god = un.od0 + gdt, goh = un.oh0 + ght, gow = un.ow0 + gwt;
+    er.grp_ok = gr < a.rows && gn < g.N && god < g.OD && goh < g.OH && gow < g.OW;
+    er.gbase = er.grp_ok ? (long long)gn * MP + ((long long)god * g.OH + goh) * g.OW + gow : 0;
+    const int m_first = un.grp * g.Mg + un.ct * BN, m_end = un.grp * g.Mg + g.Mg;
+    float* part = a.part ? a.part + (long long)un.sp * NP * g.M : nullptr;
+    uint4 zn0 = make_uint4(0, 0, 0, 0), zn1 = zn0;
+    if (vec && a.z && !part && m_first + half * 16 < m_end)
+      load_z16(a.z, er, m_first + half * 16, m_end, g.P, lane, zn0, zn1);
+    if (!bounded_wait(ptx::smem_addr(&ctl.acc_full[b]), (tcount >> 1) & 1, abort_flag)) break;
+    ptx::tc_fence_after();
+    epilogue_tile<BN, ACT>(g, a.b, a.z, a.y, part, vec, er, m_first, m_end, lane_base + b * kAccCols,
+                           half, lane, yst, zst, zn0, zn1);
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl.acc_empty[b]));
+  }
 }
 
 template <int BN>
@@ -711,122 +763,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
   } else {
     // ================================================================ epilogue (warps 0-7)
-    const int q = warp & 3;      // TMEM lane quarter
-    const int half = warp >> 2;  // which alternate 16-column groups
-    const int r = q * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-    const uint32_t yst = base + (uint32_t)S * kStageBytes + (uint32_t)warp * 2048u;
-    const uint32_t zst = yst + 1024u;
-    // this row's place in the pixel box
-    const int wt = r % a.Wt;
-    const int ht = (r / a.Wt) % a.Ht;
-    const int dt = (r / (a.Wt * a.Ht)) % a.Dt;
-    const int nb = r / (a.Wt * a.Ht * a.Dt);
-    // the 8-row group this lane moves in the vector path
-    const int gr = q * 32 + (lane & 3) * 8;
-    const int gwt = gr % a.Wt, ght = (gr / a.Wt) % a.Ht, gdt = (gr / (a.Wt * a.Ht)) % a.Dt;
-    const int gnb = gr / (a.Wt * a.Ht * a.Dt);
-    const long long NP = (long long)g.N * g.P;
-    uint32_t tcount = 0;
-    for (long long u = blockIdx.x; u < a.units; u += gridDim.x, ++tcount) {
-      if (*abort_flag) break;
-      const TmaUnit un = decode_tma_unit(u, a, g.G);
-      const uint32_t b = tcount & 1u;
-      const int gn = un.n0 + gnb, god = un.od0 + gdt, goh = un.oh0 + ght, gow = un.ow0 + gwt;
-      const bool grp_ok =
-          gr < a.rows && gn < g.N && god < g.OD && goh < g.OH && gow < g.OW;
-      const long long gpix = ((long long)god * g.OH + goh) * g.OW + gow;
-      const int mc0 = un.ct * BN;
-      // Z vectors of the next 16-column group, requested one group ahead (the first one
-      // before waiting for the accumulator) so the load latency overlaps other work
-      const bool zvec = a.vec && a.z != nullptr && a.part == nullptr;
-      uint4 zn0 = make_uint4(0, 0, 0, 0), zn1 = make_uint4(0, 0, 0, 0);
-      auto load_z = [&](int c0, uint4& z0, uint4& z1) {
-        const int mcb = mc0 + c0;
-        const long long zb = ((long long)gn * g.M + un.grp * g.Mg + mcb) * g.P + gpix;
-        const int ch0 = lane >> 2, ch1 = (lane >> 2) + 8;
-        z0 = (grp_ok && c0 < BN && mcb + ch0 < g.Mg) ? ptx::ldg_nc_v4(a.z + zb + (long long)ch0 * g.P)
-                                                    : make_uint4(0, 0, 0, 0);
-        z1 = (grp_ok && c0 < BN && mcb + ch1 < g.Mg) ? ptx::ldg_nc_v4(a.z + zb + (long long)ch1 * g.P)
-                                                    : make_uint4(0, 0, 0, 0);
-      };
-      if (zvec) load_z(half * 16, zn0, zn1);
-      if (!bounded_wait(ptx::smem_addr(&ctl.acc_full[b]), (tcount >> 1) & 1, abort_flag)) break;
-      ptx::tc_fence_after();
-      const int n = un.n0 + nb, od = un.od0 + dt, oh = un.oh0 + ht, ow = un.ow0 + wt;
-      const bool row_ok = r < a.rows && n < g.N && od < g.OD && oh < g.OH && ow < g.OW;
-      const long long obase =
-          row_ok ? (long long)n * g.M * g.P + ((long long)od * g.OH + oh) * g.OW + ow : 0;
-#pragma unroll 1
-      for (int c0 = half * 16; c0 < BN; c0 += 32) {
-        const uint4 zc0 = zn0, zc1 = zn1;
-        if (zvec && c0 + 32 < BN) load_z(c0 + 32, zn0, zn1);
-        float v[16];
-        __syncwarp();
-        ptx::tmem_ld16(lane_base + b * kAccCols + (uint32_t)c0, v);
-        const int mcb = mc0 + c0;
-        const int nvalid = min(16, g.Mg - mcb);
-        if (nvalid <= 0) continue;
-        const int m0 = un.grp * g.Mg + mcb;
-        const bool hz = a.z != nullptr, hb = a.b != nullptr;
-        uint32_t zr[16], br[16];
-        if (a.part) {
-          if (!row_ok) continue;
-          float* pp = a.part + (long long)un.sp * NP * g.M + obase + (long long)m0 * g.P;
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj)
-            if (jj < nvalid) pp[(long long)jj * g.P] = v[jj];
-          continue;
-        }
-        if (a.vec) {
-          if (hz) {
-            ptx::st_shared_v4(zst + (lane >> 2) * 64 + (lane & 3) * 16, zc0.x, zc0.y, zc0.z, zc0.w);
-            ptx::st_shared_v4(zst + ((lane >> 2) + 8) * 64 + (lane & 3) * 16, zc1.x, zc1.y, zc1.z,
-                              zc1.w);
-            __syncwarp();
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) zr[jj] = ptx::ld_shared_u16(zst + jj * 64 + lane * 2);
-          }
-          if (hb) {
-            const uint32_t bl = ptx::ld1_u16(a.b + m0 + (lane & 15), (lane & 15) < nvalid ? 1u : 0u);
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) br[jj] = __shfl_sync(0xffffffffu, bl, jj);
-          }
-#define FCONV_EPI16S(ACT) epi_stage16<ACT>(v, zr, br, hz, hb, yst + lane * 2, g.alpha, g.beta)
-          FCONV_ACT_SWITCH(g.act, FCONV_EPI16S)
-#undef FCONV_EPI16S
-          __syncwarp();
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const int ch = (lane >> 2) + 8 * t;
-            if (grp_ok && ch < nvalid) {
-              const uint4 yv = ptx::ld_shared_v4(yst + ch * 64 + (lane & 3) * 16);
-              ptx::st_global_v4(a.y + (((long long)gn * g.M + m0 + ch) * g.P + gpix), yv);
-            }
-          }
-          __syncwarp();
-          continue;
-        }
-        if (!row_ok) continue;
-        const long long yb = obase + (long long)m0 * g.P;
-        if (hz) {
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj)
-            zr[jj] = ptx::ld1_u16(a.z + yb + (long long)jj * g.P, jj < nvalid ? 1u : 0u);
-        }
-        if (hb) {
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) br[jj] = ptx::ld1_u16(a.b + m0 + jj, jj < nvalid ? 1u : 0u);
-        }
-        __half* yp = a.y + yb;
-#define FCONV_EPI16(ACT) epi_store16<ACT>(v, zr, br, hz, hb, nvalid, yp, g.P, g.alpha, g.beta)
-        FCONV_ACT_SWITCH(g.act, FCONV_EPI16)
-#undef FCONV_EPI16
-      }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl.acc_empty[b]));
-    }
+#define FCONV_EPI_LOOP(ACT) tma_epilogue<BN, ACT>(g, a, ctl, tmem, base + (uint32_t)S * kStageBytes, warp, lane)
+    FCONV_ACT_SWITCH(g.act, FCONV_EPI_LOOP)
+#undef FCONV_EPI_LOOP
   }
 
   ptx::tc_fence_before();
@@ -908,26 +847,90 @@ __global__ void __launch_bounds__(256) pack_x_scalar_kernel(const uint16_t* __re
   }
 }
 
+// X for the gather: Xc[g][n][pixel][cp], channels innermost, zero past C/group, so that
+// each 16-byte piece of a GEMM row is one aligned load. One thread per packed pixel
+// (blockIdx.y = g * N + n): the reads of each channel plane are coalesced across the
+// warp, and the warp's 16-byte writes cover one contiguous run of Xc.
+__global__ void __launch_bounds__(256) pack_cl_kernel(const uint16_t* __restrict__ x,
+                                                      uint16_t* __restrict__ xc, int N, int G,
+                                                      int Cg, int cp, int S) {
+  for (int gn = blockIdx.y; gn < G * N; gn += gridDim.y) {
+    const int gi = gn / N, n = gn - gi * N;
+    const uint16_t* src = x + ((long long)n * G + gi) * Cg * (long long)S;
+    uint16_t* dst = xc + (long long)gn * S * cp;
+    for (int sp = blockIdx.x * 256 + threadIdx.x; sp < S; sp += gridDim.x * 256) {
+      for (int c8 = 0; c8 < cp; c8 += 8) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = c8 + 2 * e;
+          const uint32_t lo = c < Cg ? (uint32_t)src[(long long)c * S + sp] : 0u;
+          const uint32_t hi = c + 1 < Cg ? (uint32_t)src[(long long)(c + 1) * S + sp] : 0u;
+          w[e] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4*>(dst + (long long)sp * cp + c8) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+  }
+}
+
+// As pack_cl_kernel for S % 8 == 0: one thread per 8 consecutive pixels and 8 channels.
+// Eight 16-byte loads (8 pixels of one channel plane each, coalesced across the warp), an
+// 8 x 8 transpose of 16-bit values in registers (byte permutes: pixel 2k takes the low
+// halves of word k of each channel pair, pixel 2k + 1 the high halves), eight 16-byte
+// stores (8 channels of one pixel each).
+__global__ void __launch_bounds__(256) pack_cl8_kernel(const uint16_t* __restrict__ x,
+                                                       uint16_t* __restrict__ xc, int N, int G,
+                                                       int Cg, int cp, int S) {
+  const int S8 = S / 8;
+  for (int gn = blockIdx.y; gn < G * N; gn += gridDim.y) {
+    const int gi = gn / N, n = gn - gi * N;
+    const uint16_t* src = x + ((long long)n * G + gi) * Cg * (long long)S;
+    uint16_t* dst = xc + (long long)gn * S * cp;
+    for (int j = blockIdx.x * 256 + threadIdx.x; j < S8; j += gridDim.x * 256) {
+      for (int c8 = 0; c8 < cp; c8 += 8) {
+        uint32_t w[8][4];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 r = make_uint4(0, 0, 0, 0);
+          if (c8 + c < Cg) r = ptx::ldg_nc_v4(src + (long long)(c8 + c) * S + 8LL * j);
+          w[c][0] = r.x; w[c][1] = r.y; w[c][2] = r.z; w[c][3] = r.w;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 lo = make_uint4(__byte_perm(w[0][k], w[1][k], 0x5410), __byte_perm(w[2][k], w[3][k], 0x5410),
+                                      __byte_perm(w[4][k], w[5][k], 0x5410), __byte_perm(w[6][k], w[7][k], 0x5410));
+          const uint4 hi = make_uint4(__byte_perm(w[0][k], w[1][k], 0x7632), __byte_perm(w[2][k], w[3][k], 0x7632),
+                                      __byte_perm(w[4][k], w[5][k], 0x7632), __byte_perm(w[6][k], w[7][k], 0x7632));
+          ptx::st_global_v4(dst + (8LL * j + 2 * k) * cp + c8, lo);
+          ptx::st_global_v4(dst + (8LL * j + 2 * k + 1) * cp + c8, hi);
+        }
+      }
+    }
+  }
+}
+
 // Weights in the GEMM's K order, zero padded to kpad columns: wp[m][k'] for k' < kpad.
 // One block per output channel: the row is staged in shared memory (16-byte loads when
 // rows are 16-byte aligned), then each thread writes 8 consecutive k' as one 16-byte
 // store, reading the permuted sources from shared memory.
-__device__ __forceinline__ int prep_src(int k, int Cg, int KV, int chan) {
-  if (chan && (Cg % 64) == 0) {  // (64-channel block, tap, channel)
+//   block64 (TMA-fed A, C/group a multiple of 64): k' = (64-channel block, tap, channel)
+//   otherwise (gathered A): k' = tap * cp + channel, zero for channels >= C/group
+__device__ __forceinline__ int prep_src(int k, int Cg, int KV, int cp, int block64) {
+  if (block64) {
+    if (k >= Cg * KV) return -1;
     const int cb = k / (64 * KV), rem = k - cb * 64 * KV;
     const int tap = rem >> 6;
     return (cb * 64 + (rem & 63)) * KV + tap;
   }
-  if (chan) {  // (tap, channel)
-    const int tap = k / Cg;
-    return (k - tap * Cg) * KV + tap;
-  }
-  return k;
+  const int tap = k / cp, c = k - tap * cp;
+  return (c < Cg && tap < KV) ? c * KV + tap : -1;
 }
 
 __global__ void __launch_bounds__(256) prep_weights_kernel(const uint16_t* __restrict__ w,
                                                            uint16_t* __restrict__ wp, int M,
-                                                           int Cg, int KV, int kpad, int chan) {
+                                                           int Cg, int KV, int kpad, int cp,
+                                                           int block64) {
   extern __shared__ uint16_t row[];
   const int m = blockIdx.x;
   const int Kg = Cg * KV;
@@ -944,8 +947,8 @@ __global__ void __launch_bounds__(256) prep_weights_kernel(const uint16_t* __res
     uint32_t e[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int k = v * 8 + j;
-      e[j] = k < Kg ? (uint32_t)row[prep_src(k, Cg, KV, chan)] : 0u;
+      const int src_k = prep_src(v * 8 + j, Cg, KV, cp, block64);
+      e[j] = src_k >= 0 ? (uint32_t)row[src_k] : 0u;
     }
     reinterpret_cast<uint4*>(dst)[v] =
         make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16), e[6] | (e[7] << 16));
@@ -992,7 +995,8 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-bool channel_inner(const ConvGeom& g) { return (g.Cg % 8) == 0; }
+// Channels per packed pixel of the gathered A operand.
+int cp_of(const ConvGeom& g) { return (g.Cg + 7) / 8 * 8; }
 
 // Pixel box of the TMA-fed kernel.
 struct TmaShape {
@@ -1028,26 +1032,27 @@ bool use_tma(const ConvGeom& g, int a_path) {
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-template <int BN, bool CHAN>
+template <int BN>
 int launch_t(const ConvGeom& g, const IgemmConfig& c, const TcArgs& ta, const CUtensorMap& tm,
              cudaStream_t s) {
+  // the gather's in-flight depth is sized for this ring (no wait on a chunk it still owes)
+  if (c.stages < 2 * gather_depth(BN)) return (int)cudaErrorInvalidValue;
   const size_t smem = igemm_tc_smem_bytes(BN, c.stages);
-  cudaError_t e = cudaFuncSetAttribute(igemm_tc_kernel<BN, CHAN>,
+  cudaError_t e = cudaFuncSetAttribute(igemm_tc_kernel<BN>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  igemm_tc_kernel<BN, CHAN><<<(unsigned)c.grid, kThreads, smem, s>>>(g, ta, tm);
+  igemm_tc_kernel<BN><<<(unsigned)c.grid, kThreads, smem, s>>>(g, ta, tm);
   return (int)cudaGetLastError();
 }
 
-template <bool CHAN>
 int launch_bn(const ConvGeom& g, const IgemmConfig& c, const TcArgs& ta, const CUtensorMap& tm,
               cudaStream_t s) {
   switch (c.tile_n) {
-    case 16: return launch_t<16, CHAN>(g, c, ta, tm, s);
-    case 32: return launch_t<32, CHAN>(g, c, ta, tm, s);
-    case 64: return launch_t<64, CHAN>(g, c, ta, tm, s);
-    case 128: return launch_t<128, CHAN>(g, c, ta, tm, s);
-    case 256: return launch_t<256, CHAN>(g, c, ta, tm, s);
+    case 16: return launch_t<16>(g, c, ta, tm, s);
+    case 32: return launch_t<32>(g, c, ta, tm, s);
+    case 64: return launch_t<64>(g, c, ta, tm, s);
+    case 128: return launch_t<128>(g, c, ta, tm, s);
+    case 256: return launch_t<256>(g, c, ta, tm, s);
     default: return (int)cudaErrorInvalidValue;
   }
 }
@@ -1078,37 +1083,39 @@ int launch_reduce(const ConvGeom& g, const IgemmConfig& c, const float* part, co
 
 }  // namespace
 
-int igemm_tc_stages(int tile_n) {
-  const int per = kBM * kBK * 2 + tile_n * kBK * 2;
-  int st = (200 * 1024) / per;
-  if (st > kMaxStages) st = kMaxStages;
-  st &= ~1;  // the two gather sets alternate chunks: an even ring
-  return st < 2 ? 2 : st;
-}
+int igemm_tc_stages(int tile_n) { return stages_for(tile_n); }
 
 size_t igemm_tc_smem_bytes(int tile_n, int stages) {
   // operand ring + 1 KB alignment slack + the epilogue warps' Y/Z staging tiles
   return (size_t)stages * (size_t)(kBM * kBK * 2 + tile_n * kBK * 2) + 1024 + 8 * 2048;
 }
 
-// Weight copy in GEMM order (when W itself cannot be read by TMA in that order).
-static bool needs_prep(const ConvGeom& g) {
-  if (channel_inner(g)) return !(g.KV == 1);  // 1x1: channel-inner order is W's order
-  return (g.Kg % 8) != 0;                       // TMA rows must be 16-byte multiples
+// Weight copy in GEMM order (when W itself cannot be read by TMA in that order): the
+// TMA-fed path needs it unless the kernel is 1x1 (then W's order is the block order);
+// the gather path unless also C/group is a multiple of 8 (no channel padding).
+static bool needs_prep(const ConvGeom& g, bool tma) {
+  if (tma) return g.KV != 1;
+  return !(g.KV == 1 && cp_of(g) == g.Cg);
 }
 
-static size_t kpad_of(const ConvGeom& g) { return round_up((size_t)g.Kg, 8); }
-
-static size_t prep_bytes(const ConvGeom& g) {
-  return needs_prep(g) ? round_up((size_t)g.M * kpad_of(g) * 2, 1024) : 0;
+// Columns of the GEMM's K (the weight copy's row length when there is one).
+static size_t kpad_of(const ConvGeom& g, bool tma) {
+  return tma ? (size_t)g.Kg : (size_t)g.KV * (size_t)cp_of(g);
 }
 
-static size_t pack_bytes(const ConvGeom& g, const IgemmConfig& c) {
-  return use_tma(g, c.a_path) ? round_up((size_t)g.N * g.C * (size_t)g.IS * 2, 1024) : 0;
+static size_t prep_bytes(const ConvGeom& g, bool tma) {
+  return needs_prep(g, tma) ? round_up((size_t)g.M * kpad_of(g, tma) * 2, 1024) : 0;
+}
+
+// Repacked X: 64-channel blocks for the TMA-fed path, channels-last for the gather.
+static size_t pack_bytes(const ConvGeom& g, bool tma) {
+  const size_t pix = (size_t)g.N * (size_t)g.IS;
+  return round_up(tma ? pix * (size_t)g.C * 2 : pix * (size_t)g.G * (size_t)cp_of(g) * 2, 1024);
 }
 
 size_t igemm_tc_workspace_bytes(const ConvGeom& g, const IgemmConfig& c) {
-  size_t b = prep_bytes(g) + pack_bytes(g, c);
+  const bool tma = use_tma(g, c.a_path);
+  size_t b = prep_bytes(g, tma) + pack_bytes(g, tma);
   if (c.split_k > 1) b += (size_t)c.split_k * (size_t)g.N * (size_t)g.M * (size_t)g.P * 4;
   return b;
 }
@@ -1116,7 +1123,8 @@ size_t igemm_tc_workspace_bytes(const ConvGeom& g, const IgemmConfig& c) {
 bool igemm_tc_tma_capable(const ConvGeom& g) { return tma_shape(g).ok; }
 
 int igemm_tc_launches(const ConvGeom& g, const IgemmConfig& c) {
-  return 1 + (needs_prep(g) ? 1 : 0) + (use_tma(g, c.a_path) ? 1 : 0) + (c.split_k > 1 ? 1 : 0);
+  const bool tma = use_tma(g, c.a_path);
+  return 2 + (needs_prep(g, tma) ? 1 : 0) + (c.split_k > 1 ? 1 : 0);
 }
 
 long long igemm_tc_mtiles(const ConvGeom& g, int a_path) {
@@ -1124,20 +1132,27 @@ long long igemm_tc_mtiles(const ConvGeom& g, int a_path) {
   return ((long long)g.N * g.P + kBM - 1) / kBM;
 }
 
+int igemm_tc_chunks(const ConvGeom& g, int a_path) {
+  return (int)((kpad_of(g, use_tma(g, a_path)) + kBK - 1) / kBK);
+}
+
+bool igemm_tc_gather_capable(const ConvGeom& g) {
+  // validity masks: depth taps in 32 bits with bit 31 free, (ky, kx) taps in 64 bits
+  if (g.KD > 31 || g.KH > 32 || g.KW > 32 || (long long)g.KH * g.KW > 64) return false;
+  if (round_up((size_t)g.KV * (size_t)(cp_of(g) / 8), 8) > (size_t)kMaxTab) return false;
+  // tap and row offsets (in packed elements, padded taps included) stay in 32-bit ints
+  const long long span = (long long)(g.ID + g.pD + 1) * (g.IH + g.pH + 1) * (g.IW + g.pW + 1);
+  if (span * cp_of(g) > INT_MAX / 2) return false;
+  if ((long long)g.M * (long long)kpad_of(g, false) > INT_MAX) return false;
+  return true;
+}
+
 bool igemm_tc_supported(const ConvGeom& g) {
   if (g.dtype != FCONV_F16) return false;
-  if (g.KD > 32 || g.KH > 32 || g.KW > 32) return false;
   if ((size_t)g.Kg * 2 > 200 * 1024) return false;  // weight row staged in shared memory
   // unit and pixel indices are decoded in 32 bits (every unit count is at most N*P*M)
   if ((long long)g.N * g.P * g.M >= 0x7fffffffLL) return false;
-  if (channel_inner(g) ? g.KV > kMaxTab : g.Kg > kMaxTab) return false;
-  // generic order: the per-k table holds ci * plane offsets in 32-bit ints
-  if (!channel_inner(g) && (long long)g.Cg * g.IS > INT_MAX / 2) return false;
-  // in-plane offsets, including those of padded taps, stay in 32-bit ints
-  const long long span = (long long)(g.ID + g.pD + 1) * (g.IH + g.pH + 1) * (g.IW + g.pW + 1);
-  if (span > INT_MAX / 2) return false;
-  if ((long long)g.M * (long long)kpad_of(g) > INT_MAX) return false;
-  return true;
+  return igemm_tc_gather_capable(g) || tma_shape(g).ok;
 }
 
 int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, void* stream) {
@@ -1145,11 +1160,12 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
   if (c.stages < 2 || c.stages > kMaxStages || (c.stages & 1)) return (int)cudaErrorInvalidValue;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return (int)cudaErrorNotSupported;
-  const bool chan = channel_inner(g);
+  const bool tma = use_tma(g, c.a_path);
   const uint16_t* wmat = (const uint16_t*)a.w;
   uint8_t* ws = (uint8_t*)a.ws;
-  const size_t pb = prep_bytes(g);
-  const int kpad = (int)kpad_of(g);
+  const size_t pb = prep_bytes(g, tma);
+  const int kpad = (int)kpad_of(g, tma);
+  const int cp = cp_of(g);
   if (pb) {
     uint16_t* wp = (uint16_t*)ws;
     const size_t rowbytes = (size_t)g.Kg * 2;
@@ -1160,25 +1176,37 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
       if (e != cudaSuccess) return (int)e;
     }
     prep_weights_kernel<<<(unsigned)g.M, 256, rowbytes, s>>>((const uint16_t*)a.w, wp, g.M, g.Cg,
-                                                             g.KV, kpad, chan ? 1 : 0);
+                                                             g.KV, kpad, cp, tma ? 1 : 0);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
     wmat = wp;
   }
-  const bool tma = use_tma(g, c.a_path);
-  const size_t xb_bytes = pack_bytes(g, c);
+  const size_t xb_bytes = pack_bytes(g, tma);
+  uint16_t* xpack = (uint16_t*)(ws + pb);
   if (tma) {
     const long long S = g.IS;
     const long long NS = (long long)g.N * S;
     if (S % 8 == 0) {
       dim3 pg((unsigned)((NS + 127) / 128), (unsigned)(g.C / 64), 1);
-      pack_x_kernel<<<pg, 256, 0, s>>>((const uint16_t*)a.x, (uint16_t*)(ws + pb), g.N, g.C, S);
+      pack_x_kernel<<<pg, 256, 0, s>>>((const uint16_t*)a.x, xpack, g.N, g.C, S);
     } else {
       long long blocks = (NS * (g.C / 8) + 255) / 256;
       if (blocks > 152LL * 32) blocks = 152LL * 32;
-      pack_x_scalar_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)a.x,
-                                                             (uint16_t*)(ws + pb), g.N, g.C, S);
+      pack_x_scalar_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)a.x, xpack, g.N,
+                                                             g.C, S);
     }
+  } else {
+    const long long planes = (long long)g.G * g.N;
+    const unsigned py = (unsigned)(planes < 65535 ? planes : 65535);
+    if (g.IS % 8 == 0) {
+      const dim3 pg((unsigned)((g.IS / 8 + 255) / 256), py, 1);
+      pack_cl8_kernel<<<pg, 256, 0, s>>>((const uint16_t*)a.x, xpack, g.N, g.G, g.Cg, cp, (int)g.IS);
+    } else {
+      const dim3 pg((unsigned)((g.IS + 255) / 256), py, 1);
+      pack_cl_kernel<<<pg, 256, 0, s>>>((const uint16_t*)a.x, xpack, g.N, g.G, g.Cg, cp, (int)g.IS);
+    }
+  }
+  {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
   }
@@ -1231,6 +1259,7 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
     t.units = sh.mtiles * g.G * t.ntiles * c.split_k;
     t.fd_split = make_fastdiv((uint32_t)c.split_k);
     t.fd_gnt = make_fastdiv((uint32_t)(g.G * t.ntiles));
+    t.fd_ntiles = make_fastdiv((uint32_t)t.ntiles);
     t.fd_nTw = make_fastdiv((uint32_t)t.nTw);
     t.fd_nTh = make_fastdiv((uint32_t)t.nTh);
     t.fd_nTd = make_fastdiv((uint32_t)t.nTd);
@@ -1248,13 +1277,15 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
   }
 
   TcArgs ta;
-  ta.x = (const uint16_t*)a.x;
+  ta.xc = xpack;
   ta.b = (const __half*)a.b;
   ta.z = (const __half*)a.z;
   ta.y = (__half*)a.y;
   ta.part = part;
   ta.stages = c.stages;
-  ta.chunks = (g.Kg + kBK - 1) / kBK;
+  ta.cp = cp;
+  ta.cp8 = cp / 8;
+  ta.chunks = (kpad + kBK - 1) / kBK;
   ta.chunks_per_split = (ta.chunks + c.split_k - 1) / c.split_k;
   ta.split = c.split_k;
   ta.ntiles = (g.Mg + c.tile_n - 1) / c.tile_n;
@@ -1265,7 +1296,9 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
   ta.fd_P = make_fastdiv((uint32_t)g.P);
   ta.fd_OW = make_fastdiv((uint32_t)g.OW);
   ta.fd_OH = make_fastdiv((uint32_t)g.OH);
-  const int err = chan ? launch_bn<true>(g, c, ta, tm, s) : launch_bn<false>(g, c, ta, tm, s);
+  ta.npieces = g.KV * (cp / 8);
+  ta.fd_ntiles = make_fastdiv((uint32_t)ta.ntiles);
+  const int err = launch_bn(g, c, ta, tm, s);
   if (err != 0 || c.split_k <= 1) return err;
   return launch_reduce(g, c, part, ta.b, ta.z, ta.y, s);
 }

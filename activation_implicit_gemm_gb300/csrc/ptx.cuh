@@ -188,46 +188,33 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)tmap) : "memory");
 }
 
-// Eight predicated 16-bit global loads at p, p + stride, ..., p + 7*stride (bytes),
-// issued back to back; each result is zero-extended into 32 bits (0 when !pred).
-__device__ __forceinline__ void ld8_u16(uint32_t (&v)[8], const void* p, long long stride,
-                                        uint32_t pred) {
+// 16 bytes from global memory through the non-coherent path when pred != 0, else zeros
+// (no access is made then, so p may point anywhere).
+__device__ __forceinline__ uint4 ld16_pred(const void* p, uint32_t pred) {
+  uint4 v;
   asm volatile(
-      "{\n\t.reg .pred q;\n\t.reg .b64 a;\n\t"
-      "setp.ne.b32 q, %10, 0;\n\t"
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %4, 0;\n\t"
       "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\tmov.b32 %3, 0;\n\t"
-      "mov.b32 %4, 0;\n\tmov.b32 %5, 0;\n\tmov.b32 %6, 0;\n\tmov.b32 %7, 0;\n\t"
-      "mov.b64 a, %8;\n\t"
-      "@q ld.global.nc.u16 %0, [a];\n\tadd.s64 a, a, %9;\n\t"
-      "@q ld.global.nc.u16 %1, [a];\n\tadd.s64 a, a, %9;\n\t"
-      "@q ld.global.nc.u16 %2, [a];\n\tadd.s64 a, a, %9;\n\t"
-      "@q ld.global.nc.u16 %3, [a];\n\tadd.s64 a, a, %9;\n\t"
-      "@q ld.global.nc.u16 %4, [a];\n\tadd.s64 a, a, %9;\n\t"
-      "@q ld.global.nc.u16 %5, [a];\n\tadd.s64 a, a, %9;\n\t"
-      "@q ld.global.nc.u16 %6, [a];\n\tadd.s64 a, a, %9;\n\t"
-      "@q ld.global.nc.u16 %7, [a];\n\t}"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-        "=r"(v[7])
-      : "l"(p), "l"(stride), "r"(pred));
+      "@q ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%5];\n\t}"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "r"(pred), "l"(p));
+  return v;
 }
 
-// Eight 16-bit global loads at p + k*stride (bytes), k = 0..7, zero-extended; no
-// predicate: the caller has checked the addresses.
-__device__ __forceinline__ void ld8_u16_nz(uint32_t (&v)[8], const void* p, long long stride) {
-  const char* c = (const char*)p;
-  asm volatile(
-      "ld.global.nc.u16 %0, [%8];\n\t"
-      "ld.global.nc.u16 %1, [%9];\n\t"
-      "ld.global.nc.u16 %2, [%10];\n\t"
-      "ld.global.nc.u16 %3, [%11];\n\t"
-      "ld.global.nc.u16 %4, [%12];\n\t"
-      "ld.global.nc.u16 %5, [%13];\n\t"
-      "ld.global.nc.u16 %6, [%14];\n\t"
-      "ld.global.nc.u16 %7, [%15];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-        "=r"(v[7])
-      : "l"(c), "l"(c + stride), "l"(c + 2 * stride), "l"(c + 3 * stride), "l"(c + 4 * stride),
-        "l"(c + 5 * stride), "l"(c + 6 * stride), "l"(c + 7 * stride));
+// Asynchronous 16-byte global -> shared copy (L1-allocating); src_bytes = 0 writes 16
+// zero bytes and reads nothing. Both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Waits until at most N of this thread's committed copy groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // One predicated 16-bit global load, zero-extended (0 when !pred).
@@ -242,16 +229,6 @@ __device__ __forceinline__ uint32_t ld1_u16(const void* p, uint32_t pred) {
 }
 
 // Pack eight zero-extended 16-bit values into 16 bytes and store them to shared memory.
-__device__ __forceinline__ void st_shared_pack8(uint32_t addr, const uint32_t* v) {
-  asm volatile(
-      "{\n\t.reg .b32 p0, p1, p2, p3;\n\t"
-      "prmt.b32 p0, %1, %2, 0x5410;\n\tprmt.b32 p1, %3, %4, 0x5410;\n\t"
-      "prmt.b32 p2, %5, %6, 0x5410;\n\tprmt.b32 p3, %7, %8, 0x5410;\n\t"
-      "st.shared.v4.b32 [%0], {p0, p1, p2, p3};\n\t}" ::"r"(addr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-      : "memory");
-}
-
 // 5-D tiled TMA load (c0 innermost).
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tmap, int c0, int c1, int c2,
                                             int c3, int c4, uint32_t bar) {
