@@ -62,15 +62,16 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kWarps = 18;
+constexpr int kWarps = 22;
 constexpr int kThreads = kWarps * 32;
-constexpr int kEpiWarp0 = 0;     // warps 0-7 (two per TMEM lane quarter)
-constexpr int kEpiWarps = 8;
-constexpr int kGatherWarp0 = 8;  // warps 8-15
-constexpr int kMmaWarp = 16;
-constexpr int kTmaWarp = 17;
+constexpr int kEpiWarp0 = 0;      // warps 0-15 (four per TMEM lane quarter)
+constexpr int kEpiWarps = 16;
+constexpr int kGatherWarp0 = 16;  // warps 16-19: one thread per tile row
+constexpr int kMmaWarp = 20;
+constexpr int kTmaWarp = 21;
+constexpr uint32_t kStagingBytes = 1024;  // per epilogue warp: [16 channels][32 pixels] f16
 constexpr int kMaxStages = 8;
-constexpr int kMaxTab = 2048;    // per-piece table entries (16-byte pieces of a GEMM row)
+constexpr int kMaxTab = 1024;    // per-copy table entries of a GEMM row
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // Shared-memory ring depth for a tile width: as many (A 16 KB + B) chunks as fit in
@@ -80,10 +81,10 @@ __host__ __device__ constexpr int stages_for(int bn) {
   const int capped = (st > kMaxStages ? kMaxStages : st) & ~1;
   return capped < 2 ? 2 : capped;
 }
-// Chunks whose copies a gather thread keeps in flight. Each set then holds at most
+// Chunks whose copies a gather thread keeps in flight. The gather then holds at most
 // depth - 1 chunks that are loaded but not yet handed to the MMA while it waits for a free
 // stage, and the stage it waits for was consumed after chunks older than all of those:
-// with stages >= 2 * depth the wait never depends on an arrival still owed by a gather set.
+// with stages > depth the wait never depends on an arrival the gather still owes.
 __host__ __device__ constexpr int gather_depth(int bn) { return stages_for(bn) / 2 < 4 ? stages_for(bn) / 2 : 4; }
 constexpr unsigned kErrWaitTimeout = 1u;
 
@@ -94,8 +95,10 @@ struct TcArgs {
   __half* y;
   float* part;          // split-K partials [split][N][M][P] (f32), or null
   int stages;
-  int cp, cp8;          // channels per packed pixel (C/group rounded up to 8), cp / 8
-  int npieces;          // KV * cp8: 16-byte pieces of a GEMM row
+  int cp;               // channels per packed pixel: 2, 4 or C/group rounded up to 8
+  int row_units;        // copies per GEMM row: KV (cp < 8, one tap each) or KV * cp / 8
+  int ytma;             // Y leaves by TMA stores of [16 channels][32 pixels] boxes
+  int upc;              // copies per 64-wide chunk: 8 (16 bytes), 16 (8 bytes), 32 (4 bytes)
   int chunks;           // ceil(KV * cp / 64)
   int chunks_per_split;
   int split;
@@ -167,6 +170,8 @@ struct EpiRows {
   long long obase;  // n * M * P + pixel index of this lane's pixel
   bool grp_ok;      // this lane's 8-pixel group exists
   long long gbase;  // n * M * P + first pixel of that group
+  bool run_ok;      // TMA-stored Y: the warp's 32-pixel run exists ...
+  int run_p, run_n; // ... and starts at pixel run_p of image run_n
 };
 
 // Z of channels mcb + lane / 4 and mcb + lane / 4 + 8 for this lane's pixel group.
@@ -181,9 +186,11 @@ __device__ __forceinline__ void load_z16(const __half* z, const EpiRows& er, int
 }
 
 // Activation of 16 pre-activation values and f16 rounding into this lane's column of the
-// staging tile (64 bytes per channel row).
+// staging tile ys[16 channels][32 pixels] (plain shared-memory accesses, so the row
+// offsets fold into the store instructions).
 template <int ACT>
-__device__ __forceinline__ void stage16(const float (&v)[16], uint32_t col, float alpha, float beta) {
+__device__ __forceinline__ void stage16(const float (&v)[16], __half* ys, int lane, float alpha,
+                                        float beta) {
   float o[16];
 #pragma unroll
   for (int jj = 0; jj < 16; ++jj) o[jj] = act_eval<ACT, true>(v[jj], alpha, beta);
@@ -191,84 +198,105 @@ __device__ __forceinline__ void stage16(const float (&v)[16], uint32_t col, floa
   for (int jj = 0; jj < 16; jj += 2) {
     // one packed conversion for two channels, then the two 2-byte stores
     const __half2 h2 = __floats2half2_rn(o[jj], o[jj + 1]);
-    ptx::st_shared_u16(col + jj * 64, __half_as_ushort(__low2half(h2)));
-    ptx::st_shared_u16(col + (jj + 1) * 64, __half_as_ushort(__high2half(h2)));
+    ys[jj * 32 + lane] = __low2half(h2);
+    ys[(jj + 1) * 32 + lane] = __high2half(h2);
   }
 }
 
+// ACT value of the split-K kernels' epilogue: raw f32 partial sums, nothing applied.
+constexpr int kActPartial = -1;
+
 // One tile's epilogue for this warp. acc = TMEM address of the warp's lane quarter in the
 // tile's accumulator buffer; channels [m_first, m_first + BN) of the tile, of which those
-// below m_end exist; part = split-K partials of this unit's split (raw sums, nothing else
-// applied) or null; zn0/zn1 = Z of the warp's first group, already requested.
+// below m_end exist; the warp takes the 16-column groups c_first, c_first + c_step, ...;
+// zn0/zn1 = Z of the warp's first group, already requested (vector path). With ACT == kActPartial, y is the f32 partial-sum array of this unit's split.
+// Compute and staging are the same for both store paths, which differ only in how Z
+// reaches the staging tile and how Y leaves it: the vector path moves 8-pixel groups as
+// 16-byte vectors, the scalar path (P % 8 != 0) moves each lane's own pixel.
 template <int BN, int ACT>
 __device__ __forceinline__ void epilogue_tile(const ConvGeom& g, const __half* b, const __half* z,
-                                              __half* y, float* part, bool vec,
-                                              const EpiRows& er, int m_first, int m_end,
-                                              uint32_t acc, int half, int lane, uint32_t yst,
-                                              uint32_t zst, uint4 zn0, uint4 zn1) {
+                                              void* y, bool vec, const EpiRows& er, int m_first,
+                                              int m_end, uint32_t acc, int c_first, int c_step,
+                                              int lane, __half* ys, uint4 zn0, uint4 zn1,
+                                              const CUtensorMap* ytm) {
   const bool hz = z != nullptr, hb = b != nullptr;
+  __half* zs = ys;  // Z passes through the same tile: each lane reads back only its own column
 #pragma unroll 1
-  for (int c0 = half * 16; c0 < BN; c0 += 32) {
+  for (int c0 = c_first; c0 < BN; c0 += c_step) {
     const int mcb = m_first + c0;
     if (mcb >= m_end) break;  // the same for the whole warp
     const int nvalid = min(16, m_end - mcb);
-    const uint4 zc0 = zn0, zc1 = zn1;
-    if (vec && hz && c0 + 32 < BN) load_z16(z, er, mcb + 32, m_end, g.P, lane, zn0, zn1);
-    uint32_t bl = 0;  // bias of channel mcb + lane % 16, requested before the accumulator
-    if (hb && !part) bl = ptx::ld1_u16(b + mcb + (lane & 15), (lane & 15) < nvalid ? 1u : 0u);
-    float v[16];
-    __syncwarp();
-    ptx::tmem_ld16(acc + (uint32_t)c0, v);
-    if (part) {
+    if constexpr (ACT == kActPartial) {
+      float v[16];
+      __syncwarp();
+      ptx::tmem_ld16(acc + (uint32_t)c0, v);
       if (er.row_ok) {
-        float* pp = part + er.obase + (long long)mcb * g.P;
+        float* pp = static_cast<float*>(y) + er.obase + (long long)mcb * g.P;
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj)
           if (jj < nvalid) pp[(long long)jj * g.P] = v[jj];
       }
       continue;
-    }
-    if (hb) {
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj)
-        v[jj] += __half2float(__ushort_as_half((unsigned short)__shfl_sync(0xffffffffu, bl, jj)));
-    }
-    if (vec) {
-      if (hz) {
-        ptx::st_shared_v4(zst + (lane >> 2) * 64 + (lane & 3) * 16, zc0.x, zc0.y, zc0.z, zc0.w);
-        ptx::st_shared_v4(zst + ((lane >> 2) + 8) * 64 + (lane & 3) * 16, zc1.x, zc1.y, zc1.z, zc1.w);
+    } else {
+      const uint4 zc0 = zn0, zc1 = zn1;
+      if (vec && hz && c0 + c_step < BN) load_z16(z, er, mcb + c_step, m_end, g.P, lane, zn0, zn1);
+      uint32_t bl = 0;  // bias of channel mcb + lane % 16, requested before the accumulator
+      if (hb) bl = ptx::ld1_u16(b + mcb + (lane & 15), (lane & 15) < nvalid ? 1u : 0u);
+      if (ytm) {
+        // the previous group's box must be read out of the staging tile before reuse
+        if (lane == 0) ptx::bulk_wait_read0();
         __syncwarp();
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj)
-          v[jj] += __half2float(__ushort_as_half((unsigned short)ptx::ld_shared_u16(zst + jj * 64 + lane * 2)));
       }
-      stage16<ACT>(v, yst + lane * 2, g.alpha, g.beta);
-      __syncwarp();
+      if (hz) {
+        if (vec) {
+          reinterpret_cast<uint4*>(zs)[(lane >> 2) * 4 + (lane & 3)] = zc0;
+          reinterpret_cast<uint4*>(zs)[((lane >> 2) + 8) * 4 + (lane & 3)] = zc1;
+        } else {
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int ch = (lane >> 2) + 8 * t;
-        if (er.grp_ok && ch < nvalid) {
-          const uint4 yv = ptx::ld_shared_v4(yst + ch * 64 + (lane & 3) * 16);
-          ptx::st_global_v4(y + er.gbase + (long long)(mcb + ch) * g.P, yv);
+          for (int jj = 0; jj < 16; ++jj)
+            zs[jj * 32 + lane] = __ushort_as_half((unsigned short)ptx::ld1_u16(
+                z + er.obase + (long long)(mcb + jj) * g.P, (er.row_ok && jj < nvalid) ? 1u : 0u));
         }
       }
+      float v[16];
       __syncwarp();
-      continue;
+      ptx::tmem_ld16(acc + (uint32_t)c0, v);
+      if (hb) {
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj)
+          v[jj] += __half2float(__ushort_as_half((unsigned short)__shfl_sync(0xffffffffu, bl, jj)));
+      }
+      if (hz) {
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) v[jj] += __half2float(zs[jj * 32 + lane]);
+      }
+      stage16<ACT>(v, ys, lane, g.alpha, g.beta);
+      if (ytm) {
+        // one TMA store of the [16 channels][32 pixels] box (16 channels inside the group)
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && er.run_ok) {
+          ptx::tma_store_3d(ytm, ptx::smem_addr(ys), er.run_p, mcb, er.run_n);
+          ptx::bulk_commit();
+        }
+        continue;
+      }
+      __syncwarp();
+      __half* yh = static_cast<__half*>(y);
+      if (vec) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int ch = (lane >> 2) + 8 * t;
+          if (er.grp_ok && ch < nvalid) {
+            const uint4 yv = reinterpret_cast<const uint4*>(ys)[ch * 4 + (lane & 3)];
+            ptx::st_global_v4(yh + er.gbase + (long long)(mcb + ch) * g.P, yv);
+          }
+        }
+      } else if (er.row_ok) {
+        for (int jj = 0; jj < nvalid; ++jj) yh[er.obase + (long long)(mcb + jj) * g.P] = ys[jj * 32 + lane];
+      }
+      __syncwarp();
     }
-    if (!er.row_ok) continue;
-    const long long yb = er.obase + (long long)mcb * g.P;
-    if (hz) {
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj)
-        v[jj] += __half2float(__ushort_as_half(
-            (unsigned short)ptx::ld1_u16(z + yb + (long long)jj * g.P, jj < nvalid ? 1u : 0u)));
-    }
-    __half h[16];
-#pragma unroll
-    for (int jj = 0; jj < 16; ++jj) h[jj] = __float2half_rn(act_eval<ACT, true>(v[jj], g.alpha, g.beta));
-#pragma unroll
-    for (int jj = 0; jj < 16; ++jj)
-      if (jj < nvalid) y[yb + (long long)jj * g.P] = h[jj];
   }
 }
 
@@ -276,15 +304,15 @@ __device__ __forceinline__ void epilogue_tile(const ConvGeom& g, const __half* b
 // q = n * P + pixel.
 template <int BN, int ACT>
 __device__ __forceinline__ void gather_epilogue(const ConvGeom& g, const TcArgs& a, SharedCtl& ctl,
-                                                uint32_t tmem, uint32_t staging, int warp, int lane) {
+                                                uint32_t tmem, uint8_t* staging, int warp, int lane,
+                                                const CUtensorMap* tmap_y) {
   constexpr uint32_t kAccCols = BN < 32 ? 32 : BN;
-  const int q4 = (warp - kEpiWarp0) & 3;     // TMEM lane quarter
-  const int half = (warp - kEpiWarp0) >> 2;  // which alternate 16-column groups
+  const int q4 = (warp - kEpiWarp0) & 3;               // TMEM lane quarter
+  const int c_first = ((warp - kEpiWarp0) >> 2) * 16;  // 16-column groups c_first + 64 k
   const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
   // 16-byte Y/Z vectors need 8-pixel groups inside one image (P % 8 == 0)
   const bool vec = (g.P % 8) == 0;
-  const uint32_t yst = staging + (uint32_t)(warp - kEpiWarp0) * 2048u;
-  const uint32_t zst = yst + 1024u;
+  __half* ys = reinterpret_cast<__half*>(staging + (warp - kEpiWarp0) * kStagingBytes);
   const long long NP = (long long)g.N * g.P;
   const long long MP = (long long)g.M * g.P;
   volatile int* abort_flag = &ctl.abort_flag;
@@ -308,24 +336,32 @@ __device__ __forceinline__ void gather_epilogue(const ConvGeom& g, const TcArgs&
       const long long gn = fast_div((uint32_t)gq, a.fd_P);
       er.gbase = gn * MP + (gq - gn * g.P);
     }
+    const long long rq = un.rt * kBM + q4 * 32;
+    er.run_ok = rq < NP;
+    er.run_n = er.run_ok ? (int)fast_div((uint32_t)rq, a.fd_P) : 0;
+    er.run_p = (int)(rq - (long long)er.run_n * g.P);
     const int m_first = un.grp * g.Mg + un.ct * BN, m_end = un.grp * g.Mg + g.Mg;
-    float* part = a.part ? a.part + (long long)un.sp * NP * g.M : nullptr;
+    void* out = a.y;
+    if constexpr (ACT == kActPartial) out = a.part + (long long)un.sp * NP * g.M;
     uint4 zn0 = make_uint4(0, 0, 0, 0), zn1 = zn0;
-    if (vec && a.z && !part && m_first + half * 16 < m_end)
-      load_z16(a.z, er, m_first + half * 16, m_end, g.P, lane, zn0, zn1);
+    if (ACT != kActPartial && vec && a.z && m_first + c_first < m_end)
+      load_z16(a.z, er, m_first + c_first, m_end, g.P, lane, zn0, zn1);
     if (!bounded_wait(ptx::smem_addr(&ctl.acc_full[b]), (tcount >> 1) & 1, abort_flag)) break;
     ptx::tc_fence_after();
-    epilogue_tile<BN, ACT>(g, a.b, a.z, a.y, part, vec, er, m_first, m_end, lane_base + b * kAccCols,
-                           half, lane, yst, zst, zn0, zn1);
+    epilogue_tile<BN, ACT>(g, a.b, a.z, out, vec, er, m_first, m_end, lane_base + b * kAccCols,
+                           c_first, 4 * 16, lane, ys, zn0, zn1,
+                           (ACT != kActPartial && a.ytma) ? tmap_y : nullptr);
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl.acc_empty[b]));
   }
+  if (a.ytma && lane == 0) ptx::bulk_wait0();  // Y stores complete before the CTA ends
 }
 
-template <int BN>
+template <int BN, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
-    igemm_tc_kernel(const ConvGeom g, const TcArgs a, const __grid_constant__ CUtensorMap tmap_w) {
+    igemm_tc_kernel(const ConvGeom g, const TcArgs a, const __grid_constant__ CUtensorMap tmap_w,
+                    const __grid_constant__ CUtensorMap tmap_y) {
   constexpr uint32_t kAccCols = BN < 32 ? 32 : BN;
   constexpr uint32_t kTmemCols = 2 * kAccCols;  // 64..512, a power of two
   constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB
@@ -335,9 +371,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   extern __shared__ uint8_t dsmem[];
   __shared__ SharedCtl ctl;
-  // per 16-byte piece p of a GEMM row (tap p / cp8, channels 8 (p % cp8) ..): {offset from
-  // the row's first packed pixel in elements, (ky * KW + kx) | kz << 8}; pieces past the
-  // end of K carry kz = 31, a bit that no row's depth mask has
+  // per copy unit p of a GEMM row (cp >= 8: tap p / (cp / 8), channels 8 (p % (cp / 8)) ..;
+  // cp < 8: tap p, all cp channels): {offset from the row's first packed pixel in
+  // elements, (ky * KW + kx) | kz << 8}; units past the end of K carry kz = 31, a bit that
+  // no row's depth mask has
   __shared__ __align__(16) int2 tab[kMaxTab];
 
   const int tid = threadIdx.x;
@@ -348,9 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long NP = (long long)g.N * g.P;
   const int HW = g.IH * g.IW;
 
-  for (int p = tid; p < a.chunks * 8 && p < kMaxTab; p += kThreads) {
-    if (p < a.npieces) {
-      const int t = p / a.cp8, c8 = p - t * a.cp8;
+  const int cp8 = a.cp >= 8 ? a.cp / 8 : 1;
+  for (int p = tid; p < a.chunks * a.upc && p < kMaxTab; p += kThreads) {
+    if (p < a.row_units) {
+      const int t = p / cp8, c8 = p - t * cp8;
       const int kx = t % g.KW, ky = (t / g.KW) % g.KH, kz = t / (g.KW * g.KH);
       tab[p] = make_int2((kz * g.dD * HW + ky * g.dH * g.IW + kx * g.dW) * a.cp + c8 * 8,
                          (ky * g.KW + kx) | (kz << 8));
@@ -382,14 +420,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ctl.tmem_base;
   volatile int* abort_flag = &ctl.abort_flag;
 
-  if (warp >= kGatherWarp0 && warp < kGatherWarp0 + 8) {
+  if (warp >= kGatherWarp0 && warp < kGatherWarp0 + 4) {
     // ================================================================ A gather
-    const int set = (warp - kGatherWarp0) >> 2;
-    const int r = ((warp - kGatherWarp0) & 3) * 32 + lane;  // tile row
+    const int r = (warp - kGatherWarp0) * 32 + lane;  // tile row
     const uint32_t swz = (uint32_t)(r & 7);
     constexpr int kDepth = gather_depth(BN);
     uint32_t it = 0, last_it = 0;
-    int pending = 0;  // chunks of this set whose copies are in flight, newest = last_it
+    int pending = 0;  // chunks whose copies are in flight, newest = last_it
     for (long long u = blockIdx.x; u < a.units; u += gridDim.x) {
       if (*abort_flag) break;
       const Unit un = decode_unit(u, a, g.G);
@@ -419,7 +456,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint16_t* xg =
           a.xc + ((long long)(un.grp * g.N + n) * g.IS + ((iz0 * g.IH + iy0) * g.IW + ix0)) * a.cp;
       for (int i = 0; i < un.nk; ++i, ++it) {
-        if ((int)(it & 1u) != set) continue;
         const int s = (int)(it % (uint32_t)S);
         if (it >= (uint32_t)S &&
             !bounded_wait(ptx::smem_addr(&ctl.empty[s]), ((it / S) - 1) & 1, abort_flag))
@@ -427,26 +463,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the chunk's eight 16-byte pieces: one validity test and one asynchronous 16-byte
         // copy each, straight into the 128-byte-swizzled row (zero fill for taps outside X,
         // pieces past K and rows past N*P)
-        const int4* tp = reinterpret_cast<const int4*>(&tab[(un.c_begin + i) * 8]);
+        const int4* tp = reinterpret_cast<const int4*>(&tab[(un.c_begin + i) * a.upc]);
         const uint32_t arow = (base + (uint32_t)s * kStageBytes + (uint32_t)r * 128u) | (swz << 4);
+        auto valid = [&](int bits) -> uint32_t {
+          return (uint32_t)(mhw >> (bits & 0xff)) & (mz >> (bits >> 8)) & 1u;
+        };
+        if (a.upc == 8) {
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const int4 t2 = tp[h];
+          for (int h = 0; h < 4; ++h) {
+            const int4 t2 = tp[h];
+            const uint32_t ok0 = valid(t2.y), ok1 = valid(t2.w);
+            ptx::cp_async16(arow ^ ((uint32_t)(2 * h) << 4), ok0 ? xg + t2.x : a.xc, ok0 ? 16u : 0u);
+            ptx::cp_async16(arow ^ ((uint32_t)(2 * h + 1) << 4), ok1 ? xg + t2.z : a.xc, ok1 ? 16u : 0u);
+          }
+        } else if (a.upc == 16) {
+          // two taps of 4 channels (8 bytes each) per 16-byte piece
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int off = e ? t2.z : t2.x, bits = e ? t2.w : t2.y;
-            const uint32_t ok = (uint32_t)(mhw >> (bits & 0xff)) & (mz >> (bits >> 8)) & 1u;
-            ptx::cp_async16(arow ^ ((uint32_t)(2 * h + e) << 4), ok ? xg + off : a.xc, ok ? 16u : 0u);
+          for (int j = 0; j < 8; ++j) {
+            const int4 t2 = tp[j];
+            const uint32_t ok0 = valid(t2.y), ok1 = valid(t2.w);
+            const uint32_t dst = arow ^ ((uint32_t)j << 4);
+            ptx::cp_async8(dst, ok0 ? xg + t2.x : a.xc, ok0 ? 8u : 0u);
+            ptx::cp_async8(dst + 8u, ok1 ? xg + t2.z : a.xc, ok1 ? 8u : 0u);
+          }
+        } else {
+          // four taps of 2 channels (4 bytes each) per 16-byte piece
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t dst = arow ^ ((uint32_t)j << 4);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int4 t2 = tp[2 * j + h];
+              const uint32_t ok0 = valid(t2.y), ok1 = valid(t2.w);
+              ptx::cp_async4(dst + 8u * h, ok0 ? xg + t2.x : a.xc, ok0 ? 4u : 0u);
+              ptx::cp_async4(dst + 8u * h + 4u, ok1 ? xg + t2.z : a.xc, ok1 ? 4u : 0u);
+            }
           }
         }
         ptx::cp_async_commit();
         last_it = it;
         if (++pending == kDepth) {
-          // the oldest chunk in flight (kDepth - 1 chunks of this set ago) has landed
+          // the oldest chunk in flight (kDepth - 1 chunks ago) has landed
           ptx::cp_async_wait<kDepth - 1>();
           ptx::fence_proxy_async_smem();
           __syncwarp();
-          const uint32_t old = it - 2u * (kDepth - 1);
+          const uint32_t old = it - (uint32_t)(kDepth - 1);
           if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl.full[old % (uint32_t)S]));
           --pending;
         }
@@ -457,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_proxy_async_smem();
     __syncwarp();
     for (int k = pending - 1; k >= 0; --k) {
-      const uint32_t old = last_it - 2u * (uint32_t)k;
+      const uint32_t old = last_it - (uint32_t)k;
       if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl.full[old % (uint32_t)S]));
     }
   } else if (warp == kTmaWarp) {
@@ -524,8 +585,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ================================================================ epilogue (warps 0-7)
     // one loop per activation, chosen once: the group loop carries no dispatch
-#define FCONV_EPI_LOOP(ACT) gather_epilogue<BN, ACT>(g, a, ctl, tmem, base + (uint32_t)S * kStageBytes, warp, lane)
-    FCONV_ACT_SWITCH(g.act, FCONV_EPI_LOOP)
+#define FCONV_EPI_LOOP(ACT) gather_epilogue<BN, ACT>(g, a, ctl, tmem, dsmem + (base - ptx::smem_addr(dsmem)) + (size_t)S * kStageBytes, warp, lane, &tmap_y)
+    if constexpr (SPLIT) {
+      FCONV_EPI_LOOP(kActPartial);
+    } else {
+      FCONV_ACT_SWITCH(g.act, FCONV_EPI_LOOP)
+    }
 #undef FCONV_EPI_LOOP
   }
 
@@ -602,14 +667,13 @@ __device__ __forceinline__ TmaUnit decode_tma_unit(long long u, const TmaArgs& a
 // Dt x Ht x Wt), row r = ((nb * Dt + dt) * Ht + ht) * Wt + wt.
 template <int BN, int ACT>
 __device__ __forceinline__ void tma_epilogue(const ConvGeom& g, const TmaArgs& a, SharedCtl& ctl,
-                                             uint32_t tmem, uint32_t staging, int warp, int lane) {
+                                             uint32_t tmem, uint8_t* staging, int warp, int lane) {
   constexpr uint32_t kAccCols = BN < 32 ? 32 : BN;
   const int q = warp & 3;      // TMEM lane quarter
   const int half = warp >> 2;  // which alternate 16-column groups
   const int r = q * 32 + lane;
   const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-  const uint32_t yst = staging + (uint32_t)warp * 2048u;
-  const uint32_t zst = yst + 1024u;
+  __half* ys = reinterpret_cast<__half*>(staging + warp * kStagingBytes);
   // this row's place in the pixel box, and that of the 8-row group this lane moves
   const int wt = r % a.Wt, ht = (r / a.Wt) % a.Ht, dt = (r / (a.Wt * a.Ht)) % a.Dt;
   const int nb = r / (a.Wt * a.Ht * a.Dt);
@@ -633,21 +697,22 @@ __device__ __forceinline__ void tma_epilogue(const ConvGeom& g, const TmaArgs& a
     er.grp_ok = gr < a.rows && gn < g.N && god < g.OD && goh < g.OH && gow < g.OW;
     er.gbase = er.grp_ok ? (long long)gn * MP + ((long long)god * g.OH + goh) * g.OW + gow : 0;
     const int m_first = un.grp * g.Mg + un.ct * BN, m_end = un.grp * g.Mg + g.Mg;
-    float* part = a.part ? a.part + (long long)un.sp * NP * g.M : nullptr;
+    void* out = a.y;
+    if constexpr (ACT == kActPartial) out = a.part + (long long)un.sp * NP * g.M;
     uint4 zn0 = make_uint4(0, 0, 0, 0), zn1 = zn0;
-    if (vec && a.z && !part && m_first + half * 16 < m_end)
+    if (ACT != kActPartial && vec && a.z && m_first + half * 16 < m_end)
       load_z16(a.z, er, m_first + half * 16, m_end, g.P, lane, zn0, zn1);
     if (!bounded_wait(ptx::smem_addr(&ctl.acc_full[b]), (tcount >> 1) & 1, abort_flag)) break;
     ptx::tc_fence_after();
-    epilogue_tile<BN, ACT>(g, a.b, a.z, a.y, part, vec, er, m_first, m_end, lane_base + b * kAccCols,
-                           half, lane, yst, zst, zn0, zn1);
+    epilogue_tile<BN, ACT>(g, a.b, a.z, out, vec, er, m_first, m_end, lane_base + b * kAccCols,
+                           half * 16, 32, lane, ys, zn0, zn1, nullptr);
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl.acc_empty[b]));
   }
 }
 
-template <int BN>
+template <int BN, bool SPLIT>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     igemm_tma_kernel(const ConvGeom g, const TmaArgs a, const __grid_constant__ CUtensorMap tmap_x,
                      const __grid_constant__ CUtensorMap tmap_w) {
@@ -763,8 +828,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
   } else {
     // ================================================================ epilogue (warps 0-7)
-#define FCONV_EPI_LOOP(ACT) tma_epilogue<BN, ACT>(g, a, ctl, tmem, base + (uint32_t)S * kStageBytes, warp, lane)
-    FCONV_ACT_SWITCH(g.act, FCONV_EPI_LOOP)
+#define FCONV_EPI_LOOP(ACT) tma_epilogue<BN, ACT>(g, a, ctl, tmem, dsmem + (base - ptx::smem_addr(dsmem)) + (size_t)S * kStageBytes, warp, lane)
+    if constexpr (SPLIT) {
+      FCONV_EPI_LOOP(kActPartial);
+    } else {
+      FCONV_ACT_SWITCH(g.act, FCONV_EPI_LOOP)
+    }
 #undef FCONV_EPI_LOOP
   }
 
@@ -859,6 +928,10 @@ __global__ void __launch_bounds__(256) pack_cl_kernel(const uint16_t* __restrict
     const uint16_t* src = x + ((long long)n * G + gi) * Cg * (long long)S;
     uint16_t* dst = xc + (long long)gn * S * cp;
     for (int sp = blockIdx.x * 256 + threadIdx.x; sp < S; sp += gridDim.x * 256) {
+      if (cp < 8) {  // 2 or 4 channels per pixel
+        for (int c = 0; c < cp; ++c) dst[(long long)sp * cp + c] = c < Cg ? src[(long long)c * S + sp] : (uint16_t)0;
+        continue;
+      }
       for (int c8 = 0; c8 < cp; c8 += 8) {
         uint32_t w[4];
 #pragma unroll
@@ -888,6 +961,29 @@ __global__ void __launch_bounds__(256) pack_cl8_kernel(const uint16_t* __restric
     const uint16_t* src = x + ((long long)n * G + gi) * Cg * (long long)S;
     uint16_t* dst = xc + (long long)gn * S * cp;
     for (int j = blockIdx.x * 256 + threadIdx.x; j < S8; j += gridDim.x * 256) {
+      if (cp < 8) {
+        // 2 or 4 channels per pixel: the same transpose, keeping the first cp channels
+        uint32_t w[4][4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 r = make_uint4(0, 0, 0, 0);
+          if (c < Cg && c < cp) r = ptx::ldg_nc_v4(src + (long long)c * S + 8LL * j);
+          w[c][0] = r.x; w[c][1] = r.y; w[c][2] = r.z; w[c][3] = r.w;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t a0 = __byte_perm(w[0][k], w[1][k], 0x5410), a1 = __byte_perm(w[0][k], w[1][k], 0x7632);
+          if (cp == 2) {
+            *reinterpret_cast<uint32_t*>(dst + (8LL * j + 2 * k) * 2) = a0;
+            *reinterpret_cast<uint32_t*>(dst + (8LL * j + 2 * k + 1) * 2) = a1;
+          } else {
+            const uint32_t b0 = __byte_perm(w[2][k], w[3][k], 0x5410), b1 = __byte_perm(w[2][k], w[3][k], 0x7632);
+            *reinterpret_cast<uint2*>(dst + (8LL * j + 2 * k) * 4) = make_uint2(a0, b0);
+            *reinterpret_cast<uint2*>(dst + (8LL * j + 2 * k + 1) * 4) = make_uint2(a1, b1);
+          }
+        }
+        continue;
+      }
       for (int c8 = 0; c8 < cp; c8 += 8) {
         uint32_t w[8][4];
 #pragma unroll
@@ -996,7 +1092,11 @@ EncodeTiledFn encode_fn() {
 }
 
 // Channels per packed pixel of the gathered A operand.
-int cp_of(const ConvGeom& g) { return (g.Cg + 7) / 8 * 8; }
+// (2 and 4 keep the zero padding of 1-4 channel inputs small: their copies are 4 or 8 bytes)
+int cp_of(const ConvGeom& g) { return g.Cg <= 2 ? 2 : g.Cg <= 4 ? 4 : (g.Cg + 7) / 8 * 8; }
+// Copy units of a GEMM row and per 64-wide chunk.
+int units_of(const ConvGeom& g) { return cp_of(g) >= 8 ? g.KV * (cp_of(g) / 8) : g.KV; }
+int upc_of(const ConvGeom& g) { return cp_of(g) >= 8 ? 8 : 64 / cp_of(g); }
 
 // Pixel box of the TMA-fed kernel.
 struct TmaShape {
@@ -1032,40 +1132,41 @@ bool use_tma(const ConvGeom& g, int a_path) {
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-template <int BN>
+template <int BN, bool SPLIT>
 int launch_t(const ConvGeom& g, const IgemmConfig& c, const TcArgs& ta, const CUtensorMap& tm,
-             cudaStream_t s) {
+             const CUtensorMap& ty, cudaStream_t s) {
   // the gather's in-flight depth is sized for this ring (no wait on a chunk it still owes)
   if (c.stages < 2 * gather_depth(BN)) return (int)cudaErrorInvalidValue;
   const size_t smem = igemm_tc_smem_bytes(BN, c.stages);
-  cudaError_t e = cudaFuncSetAttribute(igemm_tc_kernel<BN>,
+  cudaError_t e = cudaFuncSetAttribute(igemm_tc_kernel<BN, SPLIT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  igemm_tc_kernel<BN><<<(unsigned)c.grid, kThreads, smem, s>>>(g, ta, tm);
+  igemm_tc_kernel<BN, SPLIT><<<(unsigned)c.grid, kThreads, smem, s>>>(g, ta, tm, ty);
   return (int)cudaGetLastError();
 }
 
+template <bool SPLIT>
 int launch_bn(const ConvGeom& g, const IgemmConfig& c, const TcArgs& ta, const CUtensorMap& tm,
-              cudaStream_t s) {
+              const CUtensorMap& ty, cudaStream_t s) {
   switch (c.tile_n) {
-    case 16: return launch_t<16>(g, c, ta, tm, s);
-    case 32: return launch_t<32>(g, c, ta, tm, s);
-    case 64: return launch_t<64>(g, c, ta, tm, s);
-    case 128: return launch_t<128>(g, c, ta, tm, s);
-    case 256: return launch_t<256>(g, c, ta, tm, s);
+    case 16: return launch_t<16, SPLIT>(g, c, ta, tm, ty, s);
+    case 32: return launch_t<32, SPLIT>(g, c, ta, tm, ty, s);
+    case 64: return launch_t<64, SPLIT>(g, c, ta, tm, ty, s);
+    case 128: return launch_t<128, SPLIT>(g, c, ta, tm, ty, s);
+    case 256: return launch_t<256, SPLIT>(g, c, ta, tm, ty, s);
     default: return (int)cudaErrorInvalidValue;
   }
 }
 
-template <int BN>
+template <int BN, bool SPLIT>
 int launch_tma_t(const ConvGeom& g, const IgemmConfig& c, const TmaArgs& t, const CUtensorMap& tx,
                  const CUtensorMap& tw, cudaStream_t s) {
   const size_t smem = (size_t)c.stages * (size_t)(kBM * kBK * 2 + BN * kBK * 2) + 1024 +
-                      (size_t)kTmaEpiWarps * 2048;
-  cudaError_t e = cudaFuncSetAttribute(igemm_tma_kernel<BN>,
+                      (size_t)kTmaEpiWarps * kStagingBytes;
+  cudaError_t e = cudaFuncSetAttribute(igemm_tma_kernel<BN, SPLIT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  igemm_tma_kernel<BN><<<(unsigned)c.grid, kTmaThreads, smem, s>>>(g, t, tx, tw);
+  igemm_tma_kernel<BN, SPLIT><<<(unsigned)c.grid, kTmaThreads, smem, s>>>(g, t, tx, tw);
   return (int)cudaGetLastError();
 }
 
@@ -1087,20 +1188,21 @@ int igemm_tc_stages(int tile_n) { return stages_for(tile_n); }
 
 size_t igemm_tc_smem_bytes(int tile_n, int stages) {
   // operand ring + 1 KB alignment slack + the epilogue warps' Y/Z staging tiles
-  return (size_t)stages * (size_t)(kBM * kBK * 2 + tile_n * kBK * 2) + 1024 + 8 * 2048;
+  return (size_t)stages * (size_t)(kBM * kBK * 2 + tile_n * kBK * 2) + 1024 + kEpiWarps * kStagingBytes;
 }
 
 // Weight copy in GEMM order (when W itself cannot be read by TMA in that order): the
 // TMA-fed path needs it unless the kernel is 1x1 (then W's order is the block order);
-// the gather path unless also C/group is a multiple of 8 (no channel padding).
+// the gather path unless also C/group is a multiple of 8 (no channel padding, rows of
+// whole 16-byte units).
 static bool needs_prep(const ConvGeom& g, bool tma) {
   if (tma) return g.KV != 1;
-  return !(g.KV == 1 && cp_of(g) == g.Cg);
+  return !(g.KV == 1 && cp_of(g) == g.Cg && g.Cg % 8 == 0);  // TMA rows: 16-byte multiples
 }
 
 // Columns of the GEMM's K (the weight copy's row length when there is one).
 static size_t kpad_of(const ConvGeom& g, bool tma) {
-  return tma ? (size_t)g.Kg : (size_t)g.KV * (size_t)cp_of(g);
+  return tma ? (size_t)g.Kg : round_up((size_t)g.KV * (size_t)cp_of(g), 8);
 }
 
 static size_t prep_bytes(const ConvGeom& g, bool tma) {
@@ -1139,7 +1241,7 @@ int igemm_tc_chunks(const ConvGeom& g, int a_path) {
 bool igemm_tc_gather_capable(const ConvGeom& g) {
   // validity masks: depth taps in 32 bits with bit 31 free, (ky, kx) taps in 64 bits
   if (g.KD > 31 || g.KH > 32 || g.KW > 32 || (long long)g.KH * g.KW > 64) return false;
-  if (round_up((size_t)g.KV * (size_t)(cp_of(g) / 8), 8) > (size_t)kMaxTab) return false;
+  if (round_up((size_t)units_of(g), (size_t)upc_of(g)) > (size_t)kMaxTab) return false;
   // tap and row offsets (in packed elements, padded taps included) stay in 32-bit ints
   const long long span = (long long)(g.ID + g.pD + 1) * (g.IH + g.pH + 1) * (g.IW + g.pW + 1);
   if (span * cp_of(g) > INT_MAX / 2) return false;
@@ -1264,12 +1366,13 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
     t.fd_nTh = make_fastdiv((uint32_t)t.nTh);
     t.fd_nTd = make_fastdiv((uint32_t)t.nTd);
     int err;
+    const bool sp = c.split_k > 1;
     switch (c.tile_n) {
-      case 16: err = launch_tma_t<16>(g, c, t, tx, tm, s); break;
-      case 32: err = launch_tma_t<32>(g, c, t, tx, tm, s); break;
-      case 64: err = launch_tma_t<64>(g, c, t, tx, tm, s); break;
-      case 128: err = launch_tma_t<128>(g, c, t, tx, tm, s); break;
-      case 256: err = launch_tma_t<256>(g, c, t, tx, tm, s); break;
+      case 16: err = sp ? launch_tma_t<16, true>(g, c, t, tx, tm, s) : launch_tma_t<16, false>(g, c, t, tx, tm, s); break;
+      case 32: err = sp ? launch_tma_t<32, true>(g, c, t, tx, tm, s) : launch_tma_t<32, false>(g, c, t, tx, tm, s); break;
+      case 64: err = sp ? launch_tma_t<64, true>(g, c, t, tx, tm, s) : launch_tma_t<64, false>(g, c, t, tx, tm, s); break;
+      case 128: err = sp ? launch_tma_t<128, true>(g, c, t, tx, tm, s) : launch_tma_t<128, false>(g, c, t, tx, tm, s); break;
+      case 256: err = sp ? launch_tma_t<256, true>(g, c, t, tx, tm, s) : launch_tma_t<256, false>(g, c, t, tx, tm, s); break;
       default: return (int)cudaErrorInvalidValue;
     }
     if (err != 0 || c.split_k <= 1) return err;
@@ -1284,7 +1387,8 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
   ta.part = part;
   ta.stages = c.stages;
   ta.cp = cp;
-  ta.cp8 = cp / 8;
+  ta.row_units = units_of(g);
+  ta.upc = upc_of(g);
   ta.chunks = (kpad + kBK - 1) / kBK;
   ta.chunks_per_split = (ta.chunks + c.split_k - 1) / c.split_k;
   ta.split = c.split_k;
@@ -1296,9 +1400,23 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
   ta.fd_P = make_fastdiv((uint32_t)g.P);
   ta.fd_OW = make_fastdiv((uint32_t)g.OW);
   ta.fd_OH = make_fastdiv((uint32_t)g.OH);
-  ta.npieces = g.KV * (cp / 8);
   ta.fd_ntiles = make_fastdiv((uint32_t)ta.ntiles);
-  const int err = launch_bn(g, c, ta, tm, s);
+  // Y by TMA stores: 32-pixel runs inside one image (P % 32 == 0), 16-channel boxes inside one
+  // group (C_out/group % 16 == 0); split-K partials go through the plain stores
+  CUtensorMap ty;
+  std::memset(&ty, 0, sizeof(ty));
+  ta.ytma = (c.split_k <= 1 && g.P % 32 == 0 && g.Mg % 16 == 0) ? 1 : 0;
+  if (ta.ytma) {
+    cuuint64_t ydims[3] = {(cuuint64_t)g.P, (cuuint64_t)g.M, (cuuint64_t)g.N};
+    cuuint64_t ystr[2] = {(cuuint64_t)g.P * 2, (cuuint64_t)g.M * g.P * 2};
+    cuuint32_t ybox[3] = {32, 16, 1};
+    cuuint32_t yes[3] = {1, 1, 1};
+    cr = enc(&ty, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, (void*)a.y, ydims, ystr, ybox, yes,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) ta.ytma = 0;
+  }
+  const int err = c.split_k > 1 ? launch_bn<true>(g, c, ta, tm, ty, s) : launch_bn<false>(g, c, ta, tm, ty, s);
   if (err != 0 || c.split_k <= 1) return err;
   return launch_reduce(g, c, part, ta.b, ta.z, ta.y, s);
 }
