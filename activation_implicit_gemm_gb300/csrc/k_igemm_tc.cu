@@ -427,34 +427,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kDepth = gather_depth(BN);
     uint32_t it = 0, last_it = 0;
     int pending = 0;  // chunks whose copies are in flight, newest = last_it
-    for (long long u = blockIdx.x; u < a.units; u += gridDim.x) {
-      if (*abort_flag) break;
+    // where this thread's row of unit u reads X: validity masks (bit kz of mz: depth tap
+    // kz lands inside X; bit ky * KW + kx of mhw: the (ky, kx) tap does, KH * KW <= 64) and
+    // the row's first packed pixel (possibly outside X: only valid taps are read)
+    struct RowSrc {
+      uint32_t mz;
+      uint64_t mhw;
+      const uint16_t* xg;
+    };
+    auto row_src = [&](long long u) -> RowSrc {
+      RowSrc rs{0u, 0ull, a.xc};
+      if (u >= a.units) return rs;
       const Unit un = decode_unit(u, a, g.G);
       const long long q = un.rt * kBM + r;
-      const bool row_ok = q < NP;
-      int n = 0, od = 0, oh = 0, ow = 0;
-      if (row_ok) {
-        uint32_t nn, o, t1, w1, h1;
-        fast_divmod((uint32_t)q, a.fd_P, nn, o);
-        fast_divmod(o, a.fd_OW, t1, w1);
-        fast_divmod(t1, a.fd_OH, o, h1);
-        n = (int)nn; ow = (int)w1; oh = (int)h1; od = (int)o;
-      }
-      const int iz0 = od * g.sD - g.pD, iy0 = oh * g.sH - g.pH, ix0 = ow * g.sW - g.pW;
-      // bit kz of mz: depth tap kz lands inside X; bit ky * KW + kx of mhw: the (ky, kx)
-      // tap does (KH * KW <= 64)
-      uint32_t mz = 0, mx = 0;
-      uint64_t mhw = 0;
-      for (int t = 0; t < g.KD; ++t) { const int v = iz0 + t * g.dD; if (v >= 0 && v < g.ID) mz |= 1u << t; }
+      if (q >= NP) return rs;
+      uint32_t nn, o, t1, w1, h1;
+      fast_divmod((uint32_t)q, a.fd_P, nn, o);
+      fast_divmod(o, a.fd_OW, t1, w1);
+      fast_divmod(t1, a.fd_OH, o, h1);
+      const int iz0 = (int)o * g.sD - g.pD, iy0 = (int)h1 * g.sH - g.pH, ix0 = (int)w1 * g.sW - g.pW;
+      uint32_t mx = 0;
+      for (int t = 0; t < g.KD; ++t) { const int v = iz0 + t * g.dD; if (v >= 0 && v < g.ID) rs.mz |= 1u << t; }
       for (int t = 0; t < g.KW; ++t) { const int v = ix0 + t * g.dW; if (v >= 0 && v < g.IW) mx |= 1u << t; }
       for (int t = 0; t < g.KH; ++t) {
         const int v = iy0 + t * g.dH;
-        if (v >= 0 && v < g.IH) mhw |= (uint64_t)mx << (t * g.KW);
+        if (v >= 0 && v < g.IH) rs.mhw |= (uint64_t)mx << (t * g.KW);
       }
-      if (!row_ok) mz = 0;
-      // this row's first packed pixel (possibly outside X: only valid taps are read)
-      const uint16_t* xg =
-          a.xc + ((long long)(un.grp * g.N + n) * g.IS + ((iz0 * g.IH + iy0) * g.IW + ix0)) * a.cp;
+      rs.xg = a.xc + ((long long)(un.grp * g.N + (int)nn) * g.IS + ((iz0 * g.IH + iy0) * g.IW + ix0)) * a.cp;
+      return rs;
+    };
+    RowSrc cur = row_src(blockIdx.x);
+    for (long long u = blockIdx.x; u < a.units; u += gridDim.x) {
+      if (*abort_flag) break;
+      const Unit un = decode_unit(u, a, g.G);
+      const uint32_t mz = cur.mz;
+      const uint64_t mhw = cur.mhw;
+      const uint16_t* xg = cur.xg;
+      RowSrc nxt = cur;
       for (int i = 0; i < un.nk; ++i, ++it) {
         const int s = (int)(it % (uint32_t)S);
         if (it >= (uint32_t)S &&
@@ -468,23 +477,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto valid = [&](int bits) -> uint32_t {
           return (uint32_t)(mhw >> (bits & 0xff)) & (mz >> (bits >> 8)) & 1u;
         };
+        // invalid units (taps outside X, padding past K, rows past N*P) are zeros written
+        // by plain shared stores: no copy is issued for them
         if (a.upc == 8) {
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
             const int4 t2 = tp[h];
-            const uint32_t ok0 = valid(t2.y), ok1 = valid(t2.w);
-            ptx::cp_async16(arow ^ ((uint32_t)(2 * h) << 4), ok0 ? xg + t2.x : a.xc, ok0 ? 16u : 0u);
-            ptx::cp_async16(arow ^ ((uint32_t)(2 * h + 1) << 4), ok1 ? xg + t2.z : a.xc, ok1 ? 16u : 0u);
+            const uint32_t d0 = arow ^ ((uint32_t)(2 * h) << 4), d1 = arow ^ ((uint32_t)(2 * h + 1) << 4);
+            if (valid(t2.y)) ptx::cp_async16(d0, xg + t2.x, 16u); else ptx::st_shared_v4(d0, 0u, 0u, 0u, 0u);
+            if (valid(t2.w)) ptx::cp_async16(d1, xg + t2.z, 16u); else ptx::st_shared_v4(d1, 0u, 0u, 0u, 0u);
           }
         } else if (a.upc == 16) {
           // two taps of 4 channels (8 bytes each) per 16-byte piece
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const int4 t2 = tp[j];
-            const uint32_t ok0 = valid(t2.y), ok1 = valid(t2.w);
             const uint32_t dst = arow ^ ((uint32_t)j << 4);
-            ptx::cp_async8(dst, ok0 ? xg + t2.x : a.xc, ok0 ? 8u : 0u);
-            ptx::cp_async8(dst + 8u, ok1 ? xg + t2.z : a.xc, ok1 ? 8u : 0u);
+            if (valid(t2.y)) ptx::cp_async8(dst, xg + t2.x, 8u); else ptx::st_shared_v2(dst, 0u, 0u);
+            if (valid(t2.w)) ptx::cp_async8(dst + 8u, xg + t2.z, 8u); else ptx::st_shared_v2(dst + 8u, 0u, 0u);
           }
         } else {
           // four taps of 2 channels (4 bytes each) per 16-byte piece
@@ -494,14 +504,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int4 t2 = tp[2 * j + h];
-              const uint32_t ok0 = valid(t2.y), ok1 = valid(t2.w);
-              ptx::cp_async4(dst + 8u * h, ok0 ? xg + t2.x : a.xc, ok0 ? 4u : 0u);
-              ptx::cp_async4(dst + 8u * h + 4u, ok1 ? xg + t2.z : a.xc, ok1 ? 4u : 0u);
+              if (valid(t2.y)) ptx::cp_async4(dst + 8u * h, xg + t2.x, 4u); else ptx::st_shared_u32(dst + 8u * h, 0u);
+              if (valid(t2.w)) ptx::cp_async4(dst + 8u * h + 4u, xg + t2.z, 4u); else ptx::st_shared_u32(dst + 8u * h + 4u, 0u);
             }
           }
         }
         ptx::cp_async_commit();
         last_it = it;
+        // the next unit's row setup overlaps the copies in flight
+        if (i == un.nk - 1) nxt = row_src(u + gridDim.x);
         if (++pending == kDepth) {
           // the oldest chunk in flight (kDepth - 1 chunks ago) has landed
           ptx::cp_async_wait<kDepth - 1>();
@@ -512,6 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           --pending;
         }
       }
+      cur = nxt;
     }
     // hand over the chunks still in flight (also after an abort: copies always complete)
     ptx::cp_async_wait<0>();
@@ -1136,7 +1148,7 @@ template <int BN, bool SPLIT>
 int launch_t(const ConvGeom& g, const IgemmConfig& c, const TcArgs& ta, const CUtensorMap& tm,
              const CUtensorMap& ty, cudaStream_t s) {
   // the gather's in-flight depth is sized for this ring (no wait on a chunk it still owes)
-  if (c.stages < 2 * gather_depth(BN)) return (int)cudaErrorInvalidValue;
+  if (c.stages <= gather_depth(BN)) return (int)cudaErrorInvalidValue;
   const size_t smem = igemm_tc_smem_bytes(BN, c.stages);
   cudaError_t e = cudaFuncSetAttribute(igemm_tc_kernel<BN, SPLIT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
