@@ -93,6 +93,43 @@ __device__ __forceinline__ void store_block4(const float (&acc)[4][4], const T* 
             from_f32<T>(act_eval<ACT, sizeof(T) == 2>(acc[r][j] + zv[r][j], alpha, beta));
 }
 
+// Four consecutive elements starting at p (p 4-element aligned): one 8-byte (f16) or
+// 16-byte (f32) access.
+__device__ __forceinline__ void load4(const __half* p, float (&v)[4]) {
+  const uint2 r = *reinterpret_cast<const uint2*>(p);
+  const __half2 a = *reinterpret_cast<const __half2*>(&r.x), b = *reinterpret_cast<const __half2*>(&r.y);
+  v[0] = __low2float(a); v[1] = __high2float(a); v[2] = __low2float(b); v[3] = __high2float(b);
+}
+__device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
+  const float4 r = *reinterpret_cast<const float4*>(p);
+  v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w;
+}
+__device__ __forceinline__ void store4(__half* p, const float (&v)[4]) {
+  const __half2 a = __floats2half2_rn(v[0], v[1]), b = __floats2half2_rn(v[2], v[3]);
+  uint2 r;
+  r.x = *reinterpret_cast<const uint32_t*>(&a);
+  r.y = *reinterpret_cast<const uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = r;
+}
+__device__ __forceinline__ void store4(float* p, const float (&v)[4]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+
+// Activation, rounding and one vector store per row of a 4 x 4 block of whole runs.
+template <int ACT, typename T>
+__device__ __forceinline__ void store_rows4(const float (&acc)[4][4], T* __restrict__ y, long long o,
+                                            int OW, int nr, float alpha, float beta) {
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    if (r < nr) {
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = act_eval<ACT, sizeof(T) == 2>(acc[r][j], alpha, beta);
+      store4(y + o + (long long)r * OW, v);
+    }
+  }
+}
+
 // Fast path: stride 1 and dilation 1 on both axes, KH and KW known at compile time.
 // A CTA owns an output tile of TR x TC (both multiples of 4) of one (image, channel)
 // plane; each thread computes a 4 x 4 block of outputs from KH + 3 input rows of
@@ -274,18 +311,24 @@ __global__ void __launch_bounds__(256) dw_kernel_persistent(ConvGeom g, const T*
     const long long next = plane + gridDim.x;
     if (next < planes) prefetch(next);
     const long long obase = plane * g.P + (long long)oy * g.OW + ox;
+    // Z is requested before the FMAs and added after them, so its latency overlaps them
+    // (whole 4-wide runs: OW % 4 == 0 on this path, nv == 4)
     float zv[4][4];
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int r = 0; r < 4; ++r) {
+      if (z && r < nr) {
+        load4(z + obase + (long long)r * g.OW, zv[r]);
+      } else {
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        zv[r][j] = (z && r < nr && j < nv) ? to_f32(z[obase + (long long)r * g.OW + j]) : 0.0f;
+        for (int j = 0; j < 4; ++j) zv[r][j] = 0.0f;
+      }
+    }
     if (active) {
       float acc[4][4];
 #pragma unroll
       for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[r][j] = bias + zv[r][j];
+        for (int j = 0; j < 4; ++j) acc[r][j] = bias;
       const float* base = sx + oy * pitch + ox + 4;
 #pragma unroll
       for (int ir = 0; ir < 4 + KH - 1; ++ir) {
@@ -308,8 +351,11 @@ __global__ void __launch_bounds__(256) dw_kernel_persistent(ConvGeom g, const T*
           }
         }
       }
-      // Z is already in the accumulators
-#define FCONV_DW_STORE(ACT) store_block4<ACT, T>(acc, (const T*)nullptr, y, obase, g.OW, nr, nv, g.alpha, g.beta)
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[r][j] += zv[r][j];
+#define FCONV_DW_STORE(ACT) store_rows4<ACT, T>(acc, y, obase, g.OW, nr, g.alpha, g.beta)
       FCONV_ACT_SWITCH(g.act, FCONV_DW_STORE)
 #undef FCONV_DW_STORE
     }
@@ -367,7 +413,7 @@ int launch_dw_t(const ConvGeom& g, const ConvArgs& a, cudaStream_t s) {
   const bool unit = g.sW == 1 && g.dW == 1 && g.sH == 1 && g.dH == 1;
   constexpr int VE = 16 / sizeof(T);
   if (unit && g.KH == g.KW && (g.KW == 3 || g.KW == 5 || g.KW == 7) && g.OH <= 64 &&
-      g.OW <= 64 && g.IW % VE == 0 && g.IS % VE == 0 &&
+      g.OW <= 64 && g.OW % 4 == 0 && g.IW % VE == 0 && g.IS % VE == 0 &&
       (long long)g.IH * (g.IW / VE) <= 4LL * ((g.OW + 3) / 4) * ((g.OH + 3) / 4) &&
       g.IH + g.pH <= g.OH + g.KH - 1 && g.IW + g.pW + 4 <= (g.OW + 3) / 4 * 4 + 4 + g.KW + 3) {
     // persistent CTAs; the whole plane is one tile
