@@ -252,7 +252,9 @@ __global__ void __launch_bounds__(256) dw_kernel_block(ConvGeom g, const T* __re
 // dilation 1: a CTA loops over (image, channel) planes. The zero padding of the fp32
 // tile is written once (every plane has the same halo), the next plane's input rows are
 // loaded into registers while the current plane is computed, and each thread's Z values
-// are requested before its FMA loop so their latency hides behind it.
+// are requested before its FMA loop so their latency hides behind it. The plane's
+// weights sit in shared memory (rows of 8 floats, read as broadcast vectors) rather than
+// in registers, so that more CTAs fit on an SM.
 template <typename T, int KH, int KW, int MAXV>
 __global__ void __launch_bounds__(256) dw_kernel_persistent(ConvGeom g, const T* __restrict__ x,
                                                             const T* __restrict__ w,
@@ -265,12 +267,15 @@ __global__ void __launch_bounds__(256) dw_kernel_persistent(ConvGeom g, const T*
   constexpr int WV = (WIN + 3) / 4;
   constexpr int VE = 16 / sizeof(T);
   // rows of the tile: the last block row of threads reads up to row TR + KH - 2 (TR is OH
-  // rounded up to a multiple of 4)
+  // rounded up to a multiple of 4); the weights follow the tile, KH rows of 8 floats
+  // Two such buffers alternate between planes: one barrier per plane, after which the
+  // threads compute from one buffer while the next plane is written into the other.
   const int srows = TR + KH - 1;
+  const int bufsz = srows * pitch + KH * 8;
   const int ixb = -g.pW - 4;                 // input column of tile column 0
   const int nvr = g.IW / VE;                 // 16-byte vectors per input row
   const int nvec = g.IH * nvr;               // per plane
-  for (int i = threadIdx.x * 4; i < srows * pitch; i += blockDim.x * 4)
+  for (int i = threadIdx.x * 4; i < 2 * bufsz; i += blockDim.x * 4)
     *reinterpret_cast<float4*>(sx + i) = make_float4(0.f, 0.f, 0.f, 0.f);
   const int tcols = TC / 4;
   const int ty = threadIdx.x / tcols, tx = threadIdx.x - ty * tcols;
@@ -287,40 +292,51 @@ __global__ void __launch_bounds__(256) dw_kernel_persistent(ConvGeom g, const T*
       if (i < nvec) pre[u] = *reinterpret_cast<const uint4*>(xp + (long long)i * VE);
     }
   };
-  long long plane = blockIdx.x;
-  if (plane < planes) prefetch(plane);
-  for (; plane < planes; plane += gridDim.x) {
-    const int c = (int)(plane % g.C);
-    float wr[KH * KW];
-#pragma unroll
-    for (int i = 0; i < KH * KW; ++i) wr[i] = to_f32(w[(long long)c * KH * KW + i]);
-    const float bias = b ? to_f32(b[c]) : 0.0f;
-    __syncthreads();  // the previous plane's compute is done with the tile
+  // the prefetched plane's weights and input rows into buffer buf (halo stays zero)
+  auto fill = [&](float* buf, long long pl) {
+    const int c = (int)(pl % g.C);
+    float* sw = buf + srows * pitch;
+    for (int i = threadIdx.x; i < KH * 8; i += blockDim.x) {
+      const int ky = i >> 3, kx = i & 7;
+      sw[i] = kx < KW ? to_f32(w[(long long)c * KH * KW + ky * KW + kx]) : 0.0f;
+    }
 #pragma unroll
     for (int u = 0; u < MAXV; ++u) {
       const int i = threadIdx.x + u * blockDim.x;
       if (i < nvec) {
         const int iy = i / nvr, c0 = (i - iy * nvr) * VE;
         const T* e = reinterpret_cast<const T*>(&pre[u]);
-        float* d = sx + (iy + g.pH) * pitch + (c0 - ixb);
+        float* d = buf + (iy + g.pH) * pitch + (c0 - ixb);
 #pragma unroll
         for (int k = 0; k < VE; ++k) d[k] = to_f32(e[k]);
       }
     }
+  };
+  long long plane = blockIdx.x;
+  if (plane < planes) {
+    prefetch(plane);
+    __syncthreads();  // the zero fill of both buffers is complete
+    fill(sx, plane);
     __syncthreads();
-    const long long next = plane + gridDim.x;
-    if (next < planes) prefetch(next);
+    if (plane + gridDim.x < planes) prefetch(plane + gridDim.x);
+  }
+  for (int k = 0; plane < planes; plane += gridDim.x, k ^= 1) {
+    const float* cur = sx + k * bufsz;
+    const float* sw = cur + srows * pitch;
+    const int c = (int)(plane % g.C);
+    const float bias = b ? to_f32(b[c]) : 0.0f;
     const long long obase = plane * g.P + (long long)oy * g.OW + ox;
     // Z is requested before the FMAs and added after them, so its latency overlaps them
     // (whole 4-wide runs: OW % 4 == 0 on this path, nv == 4)
-    float zv[4][4];
+    uint2 zraw[4];  // the four rows' Z, as loaded (f16: 4 values; f32: converted below)
+    float4 zf[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
+      zraw[r] = make_uint2(0u, 0u);
+      zf[r] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (z && r < nr) {
-        load4(z + obase + (long long)r * g.OW, zv[r]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) zv[r][j] = 0.0f;
+        if constexpr (sizeof(T) == 2) zraw[r] = *reinterpret_cast<const uint2*>(z + obase + (long long)r * g.OW);
+        else zf[r] = *reinterpret_cast<const float4*>(z + obase + (long long)r * g.OW);
       }
     }
     if (active) {
@@ -329,7 +345,7 @@ __global__ void __launch_bounds__(256) dw_kernel_persistent(ConvGeom g, const T*
       for (int r = 0; r < 4; ++r)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[r][j] = bias;
-      const float* base = sx + oy * pitch + ox + 4;
+      const float* base = cur + oy * pitch + ox + 4;
 #pragma unroll
       for (int ir = 0; ir < 4 + KH - 1; ++ir) {
         float win[WV * 4];
@@ -343,22 +359,38 @@ __global__ void __launch_bounds__(256) dw_kernel_persistent(ConvGeom g, const T*
         for (int r = 0; r < 4; ++r) {
           const int ky = ir - r;
           if (ky < 0 || ky >= KH) continue;
+          float wv[8];
+          const float4 w0 = *reinterpret_cast<const float4*>(sw + ky * 8);
+          const float4 w1 = *reinterpret_cast<const float4*>(sw + ky * 8 + 4);
+          wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
+          wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
 #pragma unroll
-          for (int kx = 0; kx < KW; ++kx) {
-            const float wv = wr[ky * KW + kx];
+          for (int kx = 0; kx < KW; ++kx)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[r][j] = fmaf(win[j + kx], wv, acc[r][j]);
-          }
+            for (int j = 0; j < 4; ++j) acc[r][j] = fmaf(win[j + kx], wv[kx], acc[r][j]);
         }
       }
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
+      for (int r = 0; r < 4; ++r) {
+        float zr[4];
+        if constexpr (sizeof(T) == 2) {
+          const __half2 a2 = *reinterpret_cast<const __half2*>(&zraw[r].x);
+          const __half2 b2 = *reinterpret_cast<const __half2*>(&zraw[r].y);
+          zr[0] = __low2float(a2); zr[1] = __high2float(a2); zr[2] = __low2float(b2); zr[3] = __high2float(b2);
+        } else {
+          zr[0] = zf[r].x; zr[1] = zf[r].y; zr[2] = zf[r].z; zr[3] = zf[r].w;
+        }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[r][j] += zv[r][j];
+        for (int j = 0; j < 4; ++j) acc[r][j] += zr[j];
+      }
 #define FCONV_DW_STORE(ACT) store_rows4<ACT, T>(acc, y, obase, g.OW, nr, g.alpha, g.beta)
       FCONV_ACT_SWITCH(g.act, FCONV_DW_STORE)
 #undef FCONV_DW_STORE
     }
+    const long long next = plane + gridDim.x;
+    if (next < planes) fill(sx + (k ^ 1) * bufsz, next);
+    __syncthreads();  // next plane staged; everyone is done with this plane's buffer
+    if (next + gridDim.x < planes) prefetch(next + gridDim.x);
   }
 }
 
@@ -421,7 +453,7 @@ int launch_dw_t(const ConvGeom& g, const ConvArgs& a, cudaStream_t s) {
     const int TR = (g.OH + 3) / 4 * 4;
     const int threads = (TC / 4) * (TR / 4);
     const int pitch = (TC + 4 + g.KW + 3 + 3) / 4 * 4 + 4;
-    const size_t smem = (size_t)(TR + g.KH - 1) * pitch * sizeof(float);
+    const size_t smem = 2 * ((size_t)(TR + g.KH - 1) * pitch + (size_t)g.KH * 8) * sizeof(float);
     const long long planes = (long long)g.N * g.C;
     int dev = 0, sms = 152;
     cudaGetDevice(&dev);
