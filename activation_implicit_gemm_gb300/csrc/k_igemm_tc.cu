@@ -982,16 +982,23 @@ __global__ void __launch_bounds__(256) pack_cl8_kernel(const uint16_t* __restric
           if (c < Cg && c < cp) r = ptx::ldg_nc_v4(src + (long long)c * S + 8LL * j);
           w[c][0] = r.x; w[c][1] = r.y; w[c][2] = r.z; w[c][3] = r.w;
         }
+        // the thread's 8 pixels are 8 * cp contiguous elements: 16-byte stores
+        uint32_t a0[4], a1[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const uint32_t a0 = __byte_perm(w[0][k], w[1][k], 0x5410), a1 = __byte_perm(w[0][k], w[1][k], 0x7632);
-          if (cp == 2) {
-            *reinterpret_cast<uint32_t*>(dst + (8LL * j + 2 * k) * 2) = a0;
-            *reinterpret_cast<uint32_t*>(dst + (8LL * j + 2 * k + 1) * 2) = a1;
-          } else {
+          a0[k] = __byte_perm(w[0][k], w[1][k], 0x5410);  // pixel 2k, channels 0-1
+          a1[k] = __byte_perm(w[0][k], w[1][k], 0x7632);  // pixel 2k + 1
+        }
+        if (cp == 2) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            ptx::st_global_v4(dst + (8LL * j + 4 * h) * 2,
+                              make_uint4(a0[2 * h], a1[2 * h], a0[2 * h + 1], a1[2 * h + 1]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
             const uint32_t b0 = __byte_perm(w[2][k], w[3][k], 0x5410), b1 = __byte_perm(w[2][k], w[3][k], 0x7632);
-            *reinterpret_cast<uint2*>(dst + (8LL * j + 2 * k) * 4) = make_uint2(a0, b0);
-            *reinterpret_cast<uint2*>(dst + (8LL * j + 2 * k + 1) * 4) = make_uint2(a1, b1);
+            ptx::st_global_v4(dst + (8LL * j + 2 * k) * 4, make_uint4(a0[k], b0, a1[k], b1));
           }
         }
         continue;

@@ -249,7 +249,7 @@ def run_ours(args):
     traffic = load_traffic(convs[top]["case"].name)
     roofline = {"bound": tb, "achieved": round(ach, 3), "peak": pk, "unit": unit,
                 "frac": round(ach / pk, 4), "traffic": traffic,
-                "kernel": {"igemm_tc": "igemm_tc_kernel", "depthwise": "dw_kernel_fast",
+                "kernel": {"igemm_tc": "igemm_tc_kernel", "depthwise": "dw_kernel_persistent",
                            "direct": "direct_conv_kernel"}[tp.route],
                 "launch": convs[top]["case"].name, "peak_kind": f"{peaks_kind} (burst)",
                 "algorithmic_flops_per_launch": tp.flops,
