@@ -1,8 +1,11 @@
 // Internal interface between the planner (fconv_api.cpp) and the CUDA launchers.
 #pragma once
 
+#include <cuda_runtime.h>
+
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include "../../include/fconv.h"
 
@@ -61,6 +64,24 @@ int igemm_tc_chunks(const ConvGeom& g, int a_path);        // 64-wide K chunks o
 bool igemm_tc_tma_capable(const ConvGeom& g);             // TMA-fed A path possible
 bool igemm_tc_gather_capable(const ConvGeom& g);          // gathered A path possible
 int igemm_tc_launches(const ConvGeom& g, const IgemmConfig& c);  // kernels per fconv_run
+
+// Launch with programmatic stream serialization: the kernel may begin (and run up to its
+// pdl_wait()) while the previous kernel in the stream finishes.
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      void* stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return (int)cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Device error word (set by kernels whose bounded waits gave up). Reads and clears.
 int read_and_clear_device_error(void* stream, unsigned* value);

@@ -14,6 +14,7 @@
 
 #include "epilogue.cuh"
 #include "fconv_internal.h"
+#include "ptx.cuh"
 
 namespace fconv {
 
@@ -143,6 +144,8 @@ __global__ void __launch_bounds__(256) dw_kernel_block(ConvGeom g, const T* __re
                                                        const T* __restrict__ z,
                                                        T* __restrict__ y, int TR, int TC,
                                                        int tiles_r, int tiles_c, int pitch) {
+  ptx::pdl_wait();  // inputs may be the previous kernel's outputs
+  ptx::pdl_trigger();
   extern __shared__ float sx[];  // (TR + KH - 1) rows x pitch floats
   constexpr int WIN = 4 + KW - 1;
   constexpr int WV = (WIN + 3 + 3) / 4;  // 16-byte vectors covering the window (+3 offset)
@@ -262,6 +265,8 @@ __global__ void __launch_bounds__(256) dw_kernel_persistent(ConvGeom g, const T*
                                                             const T* __restrict__ z,
                                                             T* __restrict__ y, int TR, int TC,
                                                             int pitch, long long planes) {
+  ptx::pdl_wait();  // inputs may be the previous kernel's outputs
+  ptx::pdl_trigger();
   extern __shared__ float sx[];
   constexpr int WIN = 4 + KW - 1;
   constexpr int WV = (WIN + 3) / 4;
@@ -402,6 +407,8 @@ __global__ void __launch_bounds__(kDwThreads) dw_kernel_generic(ConvGeom g, cons
                                                                 const T* __restrict__ z,
                                                                 T* __restrict__ y, int band,
                                                                 int bands, int srows, int scols) {
+  ptx::pdl_wait();  // inputs may be the previous kernel's outputs
+  ptx::pdl_trigger();
   extern __shared__ float smem[];
   float* sw = smem;
   float* sx = smem + g.KH * g.KW;
@@ -466,8 +473,8 @@ int launch_dw_t(const ConvGeom& g, const ConvArgs& a, cudaStream_t s) {
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem);                  \
     long long grid = (long long)sms * (per_sm > 0 ? per_sm : 1);                                \
     if (grid > planes) grid = planes;                                                           \
-    k<<<(unsigned)grid, threads, smem, s>>>(g, x, w, b, z, y, TR, TC, pitch, planes);           \
-    return (int)cudaGetLastError();                                                             \
+    return launch_pdl(k, dim3((unsigned)grid), dim3(threads), smem, s, g, x, w, b, z, y, TR, TC, \
+                      pitch, planes);                                                           \
   }
     FCONV_DW_PERSIST(3)
     FCONV_DW_PERSIST(5)
@@ -488,8 +495,8 @@ int launch_dw_t(const ConvGeom& g, const ConvArgs& a, cudaStream_t s) {
   if (g.KW == KV) {                                                                            \
     auto k = dw_kernel_block<T, KV, KV>;                                                       \
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);          \
-    k<<<(unsigned)nblk, threads, smem, s>>>(g, x, w, b, z, y, TR, TC, tiles_r, tiles_c, pitch); \
-    return (int)cudaGetLastError();                                                            \
+    return launch_pdl(k, dim3((unsigned)nblk), dim3(threads), smem, s, g, x, w, b, z, y, TR, TC, \
+                      tiles_r, tiles_c, pitch);                                                \
   }
     FCONV_DW_BLOCK(3)
     FCONV_DW_BLOCK(5)
@@ -498,9 +505,8 @@ int launch_dw_t(const ConvGeom& g, const ConvArgs& a, cudaStream_t s) {
   }
   auto k = dw_kernel_generic<T>;
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem);
-  k<<<(unsigned)blocks, kDwThreads, L.smem, s>>>(g, x, w, b, z, y, L.band, L.bands, L.srows,
-                                                  L.scols);
-  return (int)cudaGetLastError();
+  return launch_pdl(k, dim3((unsigned)blocks), dim3(kDwThreads), L.smem, s, g, x, w, b, z, y, L.band,
+                    L.bands, L.srows, L.scols);
 }
 
 }  // namespace

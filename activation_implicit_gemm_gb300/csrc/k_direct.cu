@@ -12,6 +12,7 @@
 
 #include "epilogue.cuh"
 #include "fconv_internal.h"
+#include "ptx.cuh"
 
 namespace fconv {
 
@@ -28,7 +29,16 @@ __global__ void __launch_bounds__(256) direct_conv_kernel(ConvGeom g, const T* _
                                                           const T* __restrict__ w,
                                                           const T* __restrict__ b,
                                                           const T* __restrict__ z,
-                                                          T* __restrict__ y, long long total) {
+                                                          T* __restrict__ y, long long total,
+                                                          int w_in_smem) {
+  extern __shared__ float wsm[];  // W widened to f32, when it fits
+  ptx::pdl_wait();
+  ptx::pdl_trigger();
+  if (w_in_smem) {
+    const int wcount = g.M * g.Cg * g.KV;  // at most 8192 when staged
+    for (int i = threadIdx.x; i < wcount; i += blockDim.x) wsm[i] = to_f32(w[i]);
+    __syncthreads();
+  }
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
     const long long o = idx % g.P;
@@ -47,15 +57,22 @@ __global__ void __launch_bounds__(256) direct_conv_kernel(ConvGeom g, const T* _
     float acc = 0.0f;
     for (int ci = 0; ci < g.Cg; ++ci) {
       const T* xp = x + ((long long)n * g.C + (long long)grp * g.Cg + ci) * g.IS;
-      const T* wp = w + ((long long)m * g.Cg + ci) * g.KV;
+      const long long woff = ((long long)m * g.Cg + ci) * g.KV;
       for (int kz = z0; kz < z1; ++kz) {
         const int iz = iz0 + kz * g.dD;
         for (int ky = y0; ky < y1; ++ky) {
           const int iy = iy0 + ky * g.dH;
           const T* xrow = xp + ((long long)iz * g.IH + iy) * g.IW + ix0;
-          const T* wrow = wp + (kz * g.KH + ky) * g.KW;
+          const long long wr = woff + (kz * g.KH + ky) * g.KW;
+          if (w_in_smem) {
+            const float* wrow = wsm + wr;
 #pragma unroll 4
-          for (int kx = x0; kx < x1; ++kx) acc = fmaf(to_f32(xrow[kx * g.dW]), to_f32(wrow[kx]), acc);
+            for (int kx = x0; kx < x1; ++kx) acc = fmaf(to_f32(xrow[kx * g.dW]), wrow[kx], acc);
+          } else {
+            const T* wrow = w + wr;
+#pragma unroll 4
+            for (int kx = x0; kx < x1; ++kx) acc = fmaf(to_f32(xrow[kx * g.dW]), to_f32(wrow[kx]), acc);
+          }
         }
       }
     }
@@ -73,16 +90,17 @@ int launch_direct(const ConvGeom& g, const ConvArgs& a, void* stream) {
   if (blocks > 152LL * 64) blocks = 152LL * 64;
   if (blocks < 1) blocks = 1;
   cudaStream_t s = (cudaStream_t)stream;
-  if (g.dtype == FCONV_F16) {
-    direct_conv_kernel<__half><<<(unsigned)blocks, threads, 0, s>>>(
-        g, (const __half*)a.x, (const __half*)a.w, (const __half*)a.b, (const __half*)a.z,
-        (__half*)a.y, total);
-  } else {
-    direct_conv_kernel<float><<<(unsigned)blocks, threads, 0, s>>>(
-        g, (const float*)a.x, (const float*)a.w, (const float*)a.b, (const float*)a.z,
-        (float*)a.y, total);
-  }
-  return (int)cudaGetLastError();
+  // W (all of it, widened to f32) is staged in shared memory when it takes at most 32 KB
+  const long long wbytes = (long long)g.M * g.Cg * g.KV * 4;
+  const int w_in_smem = wbytes <= 32 * 1024 ? 1 : 0;
+  const size_t smem = w_in_smem ? (size_t)wbytes : 0;
+  if (g.dtype == FCONV_F16)
+    return launch_pdl(direct_conv_kernel<__half>, dim3((unsigned)blocks), dim3(threads), smem, s, g,
+                      (const __half*)a.x, (const __half*)a.w, (const __half*)a.b,
+                      (const __half*)a.z, (__half*)a.y, total, w_in_smem);
+  return launch_pdl(direct_conv_kernel<float>, dim3((unsigned)blocks), dim3(threads), smem, s, g,
+                    (const float*)a.x, (const float*)a.w, (const float*)a.b, (const float*)a.z,
+                    (float*)a.y, total, w_in_smem);
 }
 
 }  // namespace fconv

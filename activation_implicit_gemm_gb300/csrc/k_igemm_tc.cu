@@ -62,13 +62,14 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kWarps = 22;
+constexpr int kWarps = 26;
 constexpr int kThreads = kWarps * 32;
 constexpr int kEpiWarp0 = 0;      // warps 0-15 (four per TMEM lane quarter)
 constexpr int kEpiWarps = 16;
-constexpr int kGatherWarp0 = 16;  // warps 16-19: one thread per tile row
-constexpr int kMmaWarp = 20;
-constexpr int kTmaWarp = 21;
+constexpr int kGatherWarp0 = 16;  // warps 16-23: two sets of four, one thread per tile row
+constexpr int kGatherWarps = 8;
+constexpr int kMmaWarp = 24;
+constexpr int kTmaWarp = 25;
 constexpr uint32_t kStagingBytes = 1024;  // per epilogue warp: [16 channels][32 pixels] f16
 constexpr int kMaxStages = 8;
 constexpr int kMaxTab = 1024;    // per-copy table entries of a GEMM row
@@ -81,10 +82,12 @@ __host__ __device__ constexpr int stages_for(int bn) {
   const int capped = (st > kMaxStages ? kMaxStages : st) & ~1;
   return capped < 2 ? 2 : capped;
 }
-// Chunks whose copies a gather thread keeps in flight. The gather then holds at most
-// depth - 1 chunks that are loaded but not yet handed to the MMA while it waits for a free
-// stage, and the stage it waits for was consumed after chunks older than all of those:
-// with stages > depth the wait never depends on an arrival the gather still owes.
+// Chunks whose copies a gather thread keeps in flight. Two gather sets take the chunks of
+// even and odd sequence number; a set waiting for a free stage holds at most depth - 1
+// chunks that are loaded but not yet handed to the MMA, all newer than 2 * depth chunks
+// before the one it waits for. The stage it waits for was last used S chunks before: with
+// S >= 2 * depth that chunk is older than every chunk either set still owes, so the wait
+// never depends on an arrival a gather set still owes.
 __host__ __device__ constexpr int gather_depth(int bn) { return stages_for(bn) / 2 < 4 ? stages_for(bn) / 2 : 4; }
 constexpr unsigned kErrWaitTimeout = 1u;
 
@@ -133,6 +136,23 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
       }
     }
   }
+}
+
+// Bit t set when tap t of an axis lands inside X: 0 <= i0 + t * d < n, for k <= 32 taps.
+__device__ __forceinline__ uint32_t tap_mask(int i0, int d, int n, int k) {
+  if (d == 1) {
+    const int lo = i0 < 0 ? -i0 : 0;
+    const int hi = min(k - 1, n - 1 - i0);
+    if (hi < lo) return 0u;
+    const uint32_t upto = hi >= 31 ? 0xffffffffu : (2u << hi) - 1u;
+    return upto & ~((1u << lo) - 1u);
+  }
+  uint32_t m = 0;
+  for (int t = 0; t < k; ++t) {
+    const int v = i0 + t * d;
+    if (v >= 0 && v < n) m |= 1u << t;
+  }
+  return m;
 }
 
 struct Unit {
@@ -419,73 +439,91 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   volatile int* abort_flag = &ctl.abort_flag;
+  // everything above touched no global memory; the prologue's outputs (and X, W, B, Z) are
+  // read only after the previous kernel has completed
+  ptx::pdl_wait();
 
-  if (warp >= kGatherWarp0 && warp < kGatherWarp0 + 4) {
+  if (warp >= kGatherWarp0 && warp < kGatherWarp0 + kGatherWarps) {
     // ================================================================ A gather
-    const int r = (warp - kGatherWarp0) * 32 + lane;  // tile row
+    const uint32_t set = (uint32_t)(warp - kGatherWarp0) >> 2;  // takes chunks it % 2 == set
+    const int r = ((warp - kGatherWarp0) & 3) * 32 + lane;       // tile row
     const uint32_t swz = (uint32_t)(r & 7);
     constexpr int kDepth = gather_depth(BN);
+    // With a single chunk of K every stage always holds chunk 0, so the units past the end
+    // of K are zero in every stage: they are written once here and skipped afterwards.
+    const int pad_from = a.chunks == 1 ? a.row_units : INT_MAX;
+    if (a.chunks == 1) {
+      const int ub = a.upc == 8 ? 16 : a.upc == 16 ? 8 : 4;  // bytes per unit
+      for (int st = (int)set; st < S; st += 2)
+        for (int p = a.row_units; p < a.upc; ++p) {
+          const uint32_t piece = (uint32_t)(p * ub) >> 4, off = (uint32_t)(p * ub) & 15u;
+          const uint32_t dst = ((base + (uint32_t)st * kStageBytes + (uint32_t)r * 128u) | (swz << 4)) ^ (piece << 4);
+          if (ub == 16) ptx::st_shared_v4(dst, 0u, 0u, 0u, 0u);
+          else if (ub == 8) ptx::st_shared_v2(dst + off, 0u, 0u);
+          else ptx::st_shared_u32(dst + off, 0u);
+        }
+    }
     uint32_t it = 0, last_it = 0;
-    int pending = 0;  // chunks whose copies are in flight, newest = last_it
-    // where this thread's row of unit u reads X: validity masks (bit kz of mz: depth tap
-    // kz lands inside X; bit ky * KW + kx of mhw: the (ky, kx) tap does, KH * KW <= 64) and
-    // the row's first packed pixel (possibly outside X: only valid taps are read)
-    struct RowSrc {
-      uint32_t mz;
-      uint64_t mhw;
-      const uint16_t* xg;
-    };
-    auto row_src = [&](long long u) -> RowSrc {
-      RowSrc rs{0u, 0ull, a.xc};
-      if (u >= a.units) return rs;
-      const Unit un = decode_unit(u, a, g.G);
-      const long long q = un.rt * kBM + r;
-      if (q >= NP) return rs;
-      uint32_t nn, o, t1, w1, h1;
-      fast_divmod((uint32_t)q, a.fd_P, nn, o);
-      fast_divmod(o, a.fd_OW, t1, w1);
-      fast_divmod(t1, a.fd_OH, o, h1);
-      const int iz0 = (int)o * g.sD - g.pD, iy0 = (int)h1 * g.sH - g.pH, ix0 = (int)w1 * g.sW - g.pW;
-      uint32_t mx = 0;
-      for (int t = 0; t < g.KD; ++t) { const int v = iz0 + t * g.dD; if (v >= 0 && v < g.ID) rs.mz |= 1u << t; }
-      for (int t = 0; t < g.KW; ++t) { const int v = ix0 + t * g.dW; if (v >= 0 && v < g.IW) mx |= 1u << t; }
-      for (int t = 0; t < g.KH; ++t) {
-        const int v = iy0 + t * g.dH;
-        if (v >= 0 && v < g.IH) rs.mhw |= (uint64_t)mx << (t * g.KW);
-      }
-      rs.xg = a.xc + ((long long)(un.grp * g.N + (int)nn) * g.IS + ((iz0 * g.IH + iy0) * g.IW + ix0)) * a.cp;
-      return rs;
-    };
-    RowSrc cur = row_src(blockIdx.x);
-    for (long long u = blockIdx.x; u < a.units; u += gridDim.x) {
+    int pending = 0;  // own chunks whose copies are in flight, newest = last_it
+    bool stop = false;
+    for (long long u = blockIdx.x; u < a.units && !stop; u += gridDim.x) {
       if (*abort_flag) break;
       const Unit un = decode_unit(u, a, g.G);
-      const uint32_t mz = cur.mz;
-      const uint64_t mhw = cur.mhw;
-      const uint16_t* xg = cur.xg;
-      RowSrc nxt = cur;
-      for (int i = 0; i < un.nk; ++i, ++it) {
-        const int s = (int)(it % (uint32_t)S);
-        if (it >= (uint32_t)S &&
-            !bounded_wait(ptx::smem_addr(&ctl.empty[s]), ((it / S) - 1) & 1, abort_flag))
+      const int first = (int)((it & 1u) ^ set);  // this set's first chunk of the unit
+      if (first >= un.nk) {
+        it += (uint32_t)un.nk;
+        continue;
+      }
+      // where this thread's row reads X: validity masks (bit kz of mz: depth tap kz lands
+      // inside X; bit ky * KW + kx of mhw: the (ky, kx) tap does, KH * KW <= 64) and the
+      // row's first packed pixel (possibly outside X: only valid taps are read)
+      uint32_t mz = 0;
+      uint64_t mhw = 0;
+      const uint16_t* xg = a.xc;
+      {
+        const long long q = un.rt * kBM + r;
+        if (q < NP) {
+          uint32_t nn, o, t1, w1, h1;
+          fast_divmod((uint32_t)q, a.fd_P, nn, o);
+          fast_divmod(o, a.fd_OW, t1, w1);
+          fast_divmod(t1, a.fd_OH, o, h1);
+          const int iz0 = (int)o * g.sD - g.pD, iy0 = (int)h1 * g.sH - g.pH, ix0 = (int)w1 * g.sW - g.pW;
+          mz = tap_mask(iz0, g.dD, g.ID, g.KD);
+          const uint32_t mx = tap_mask(ix0, g.dW, g.IW, g.KW);
+          const uint32_t my = tap_mask(iy0, g.dH, g.IH, g.KH);
+          if (mx) {
+            for (uint32_t m = my; m; m &= m - 1) mhw |= (uint64_t)mx << ((__ffs(m) - 1) * g.KW);
+          }
+          xg = a.xc + ((long long)(un.grp * g.N + (int)nn) * g.IS + ((iz0 * g.IH + iy0) * g.IW + ix0)) * a.cp;
+        }
+      }
+      auto valid = [&](int bits) -> uint32_t {
+        return (uint32_t)(mhw >> (bits & 0xff)) & (mz >> (bits >> 8)) & 1u;
+      };
+      for (int i = first; i < un.nk; i += 2) {
+        const uint32_t itc = it + (uint32_t)i;
+        const int s = (int)(itc % (uint32_t)S);
+        if (itc >= (uint32_t)S &&
+            !bounded_wait(ptx::smem_addr(&ctl.empty[s]), ((itc / S) - 1) & 1, abort_flag)) {
+          stop = true;
           break;
-        // the chunk's eight 16-byte pieces: one validity test and one asynchronous 16-byte
-        // copy each, straight into the 128-byte-swizzled row (zero fill for taps outside X,
-        // pieces past K and rows past N*P)
+        }
+        // the chunk's units: one validity test and one asynchronous copy each, straight
+        // into the 128-byte-swizzled row; invalid units (taps outside X, padding past K, rows
+        // past N*P) are zeros written by plain shared stores
         const int4* tp = reinterpret_cast<const int4*>(&tab[(un.c_begin + i) * a.upc]);
         const uint32_t arow = (base + (uint32_t)s * kStageBytes + (uint32_t)r * 128u) | (swz << 4);
-        auto valid = [&](int bits) -> uint32_t {
-          return (uint32_t)(mhw >> (bits & 0xff)) & (mz >> (bits >> 8)) & 1u;
-        };
-        // invalid units (taps outside X, padding past K, rows past N*P) are zeros written
-        // by plain shared stores: no copy is issued for them
         if (a.upc == 8) {
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
             const int4 t2 = tp[h];
             const uint32_t d0 = arow ^ ((uint32_t)(2 * h) << 4), d1 = arow ^ ((uint32_t)(2 * h + 1) << 4);
-            if (valid(t2.y)) ptx::cp_async16(d0, xg + t2.x, 16u); else ptx::st_shared_v4(d0, 0u, 0u, 0u, 0u);
-            if (valid(t2.w)) ptx::cp_async16(d1, xg + t2.z, 16u); else ptx::st_shared_v4(d1, 0u, 0u, 0u, 0u);
+            if (2 * h < pad_from) {
+              if (valid(t2.y)) ptx::cp_async16(d0, xg + t2.x, 16u); else ptx::st_shared_v4(d0, 0u, 0u, 0u, 0u);
+            }
+            if (2 * h + 1 < pad_from) {
+              if (valid(t2.w)) ptx::cp_async16(d1, xg + t2.z, 16u); else ptx::st_shared_v4(d1, 0u, 0u, 0u, 0u);
+            }
           }
         } else if (a.upc == 16) {
           // two taps of 4 channels (8 bytes each) per 16-byte piece
@@ -493,8 +531,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 8; ++j) {
             const int4 t2 = tp[j];
             const uint32_t dst = arow ^ ((uint32_t)j << 4);
-            if (valid(t2.y)) ptx::cp_async8(dst, xg + t2.x, 8u); else ptx::st_shared_v2(dst, 0u, 0u);
-            if (valid(t2.w)) ptx::cp_async8(dst + 8u, xg + t2.z, 8u); else ptx::st_shared_v2(dst + 8u, 0u, 0u);
+            if (2 * j < pad_from) {
+              if (valid(t2.y)) ptx::cp_async8(dst, xg + t2.x, 8u); else ptx::st_shared_v2(dst, 0u, 0u);
+            }
+            if (2 * j + 1 < pad_from) {
+              if (valid(t2.w)) ptx::cp_async8(dst + 8u, xg + t2.z, 8u); else ptx::st_shared_v2(dst + 8u, 0u, 0u);
+            }
           }
         } else {
           // four taps of 2 channels (4 bytes each) per 16-byte piece
@@ -504,33 +546,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int4 t2 = tp[2 * j + h];
-              if (valid(t2.y)) ptx::cp_async4(dst + 8u * h, xg + t2.x, 4u); else ptx::st_shared_u32(dst + 8u * h, 0u);
-              if (valid(t2.w)) ptx::cp_async4(dst + 8u * h + 4u, xg + t2.z, 4u); else ptx::st_shared_u32(dst + 8u * h + 4u, 0u);
+              if (4 * j + 2 * h < pad_from) {
+                if (valid(t2.y)) ptx::cp_async4(dst + 8u * h, xg + t2.x, 4u); else ptx::st_shared_u32(dst + 8u * h, 0u);
+              }
+              if (4 * j + 2 * h + 1 < pad_from) {
+                if (valid(t2.w)) ptx::cp_async4(dst + 8u * h + 4u, xg + t2.z, 4u); else ptx::st_shared_u32(dst + 8u * h + 4u, 0u);
+              }
             }
           }
         }
         ptx::cp_async_commit();
-        last_it = it;
-        // the next unit's row setup overlaps the copies in flight
-        if (i == un.nk - 1) nxt = row_src(u + gridDim.x);
+        last_it = itc;
         if (++pending == kDepth) {
-          // the oldest chunk in flight (kDepth - 1 chunks ago) has landed
+          // this set's oldest chunk in flight (kDepth - 1 own chunks ago) has landed
           ptx::cp_async_wait<kDepth - 1>();
           ptx::fence_proxy_async_smem();
           __syncwarp();
-          const uint32_t old = it - (uint32_t)(kDepth - 1);
+          const uint32_t old = itc - 2u * (uint32_t)(kDepth - 1);
           if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl.full[old % (uint32_t)S]));
           --pending;
         }
       }
-      cur = nxt;
+      it += (uint32_t)un.nk;
     }
     // hand over the chunks still in flight (also after an abort: copies always complete)
     ptx::cp_async_wait<0>();
     ptx::fence_proxy_async_smem();
     __syncwarp();
     for (int k = pending - 1; k >= 0; --k) {
-      const uint32_t old = last_it - (uint32_t)k;
+      const uint32_t old = last_it - 2u * (uint32_t)k;
       if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl.full[old % (uint32_t)S]));
     }
   } else if (warp == kTmaWarp) {
@@ -606,6 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #undef FCONV_EPI_LOOP
   }
 
+  ptx::pdl_trigger();  // this CTA's work is done: the next kernel may start
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -770,6 +815,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   volatile int* abort_flag = &ctl.abort_flag;
+  ptx::pdl_wait();  // the repacked X and the weight copy come from the prologue launch
 
   if (warp == kTmaLoadWarp) {
     // ================================================================ TMA producer
@@ -849,6 +895,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 #undef FCONV_EPI_LOOP
   }
 
+  ptx::pdl_trigger();
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == kTmaMmaWarp) {
@@ -858,19 +905,24 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- prologue
+// Everything the main kernel reads in a layout of its own is written by ONE launch,
+// prologue_kernel: its first `wblocks` blocks write the weight copy (one output channel
+// each), the others repack X. Both parts only move data.
+
 // X (N, C, spatial S) -> Xb[c/64][n][s][64]. Block (x, cb) moves 64 channels of the
 // flattened positions q = n*S + s in [128x, 128x + 128): four 16-byte loads per thread
 // (8 positions of one channel), all in flight, into a shared tile, then four 16-byte
 // stores per thread (8 channels of one position). Needs S % 8 == 0 (a load never
-// straddles two images); otherwise the scalar variant below is used.
-__global__ void __launch_bounds__(256) pack_x_kernel(const uint16_t* __restrict__ x,
-                                                     uint16_t* __restrict__ xb, int N, int C,
-                                                     long long S) {
-  constexpr int kPitch = 138;  // halves per channel row: 16-byte rows, few bank conflicts
-  __shared__ __align__(16) uint16_t t[64 * kPitch];
+// straddles two images); otherwise pack_x_scalar is used.
+constexpr int kPackPitch = 138;  // halves per channel row: 16-byte rows, few bank conflicts
+constexpr size_t kPackSmem = 64 * kPackPitch * 2;
+
+__device__ __forceinline__ void pack_x_block(const uint16_t* __restrict__ x, uint16_t* __restrict__ xb,
+                                             int N, int C, long long S, long long bx, int cb,
+                                             uint16_t* t) {
   const long long NS = (long long)N * S;
-  const long long q0 = (long long)blockIdx.x * 128;
-  const int cb = blockIdx.y;
+  const long long q0 = bx * 128;
   uint4 buf[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -887,7 +939,7 @@ __global__ void __launch_bounds__(256) pack_x_kernel(const uint16_t* __restrict_
   for (int i = 0; i < 4; ++i) {
     const int v = threadIdx.x + 256 * i;
     const int c = v >> 4, pv = v & 15;
-    uint32_t* d = reinterpret_cast<uint32_t*>(t + c * kPitch + pv * 8);  // 4-byte aligned
+    uint32_t* d = reinterpret_cast<uint32_t*>(t + c * kPackPitch + pv * 8);  // 4-byte aligned
     d[0] = buf[i].x; d[1] = buf[i].y; d[2] = buf[i].z; d[3] = buf[i].w;
   }
   __syncthreads();
@@ -900,19 +952,18 @@ __global__ void __launch_bounds__(256) pack_x_kernel(const uint16_t* __restrict_
     uint32_t w[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      w[e] = (uint32_t)t[(8 * part + 2 * e) * kPitch + p] |
-             ((uint32_t)t[(8 * part + 2 * e + 1) * kPitch + p] << 16);
+      w[e] = (uint32_t)t[(8 * part + 2 * e) * kPackPitch + p] |
+             ((uint32_t)t[(8 * part + 2 * e + 1) * kPackPitch + p] << 16);
     *reinterpret_cast<uint4*>(dst + (long long)p * 64 + 8 * part) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
-// Scalar repack for S % 8 != 0: one thread per (position, 8 channels).
-__global__ void __launch_bounds__(256) pack_x_scalar_kernel(const uint16_t* __restrict__ x,
-                                                            uint16_t* __restrict__ xb, int N, int C,
-                                                            long long S) {
+// Scalar repack for S % 8 != 0: one thread per (position, 8 channels), block bi of nb.
+__device__ __forceinline__ void pack_x_scalar(const uint16_t* __restrict__ x, uint16_t* __restrict__ xb,
+                                              int N, int C, long long S, long long bi, long long nb) {
   const long long NS = (long long)N * S;
   const long long total = NS * (C / 8);
-  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += (long long)gridDim.x * 256) {
+  for (long long i = bi * 256 + threadIdx.x; i < total; i += nb * 256) {
     const long long q = i % NS;
     const int c8 = (int)(i / NS);  // group of 8 channels
     const long long n = q / S, sp = q - n * S;
@@ -930,16 +981,16 @@ __global__ void __launch_bounds__(256) pack_x_scalar_kernel(const uint16_t* __re
 
 // X for the gather: Xc[g][n][pixel][cp], channels innermost, zero past C/group, so that
 // each 16-byte piece of a GEMM row is one aligned load. One thread per packed pixel
-// (blockIdx.y = g * N + n): the reads of each channel plane are coalesced across the
-// warp, and the warp's 16-byte writes cover one contiguous run of Xc.
-__global__ void __launch_bounds__(256) pack_cl_kernel(const uint16_t* __restrict__ x,
-                                                      uint16_t* __restrict__ xc, int N, int G,
-                                                      int Cg, int cp, int S) {
-  for (int gn = blockIdx.y; gn < G * N; gn += gridDim.y) {
+// (plane gn = g * N + n from `by` in steps of `ny`): the reads of each channel plane are
+// coalesced across the warp, and the warp's 16-byte writes cover one run of Xc.
+__device__ __forceinline__ void pack_cl(const uint16_t* __restrict__ x, uint16_t* __restrict__ xc,
+                                        int N, int G, int Cg, int cp, int S, int bx, int nx,
+                                        int by, int ny) {
+  for (int gn = by; gn < G * N; gn += ny) {
     const int gi = gn / N, n = gn - gi * N;
     const uint16_t* src = x + ((long long)n * G + gi) * Cg * (long long)S;
     uint16_t* dst = xc + (long long)gn * S * cp;
-    for (int sp = blockIdx.x * 256 + threadIdx.x; sp < S; sp += gridDim.x * 256) {
+    for (int sp = bx * 256 + threadIdx.x; sp < S; sp += nx * 256) {
       if (cp < 8) {  // 2 or 4 channels per pixel
         for (int c = 0; c < cp; ++c) dst[(long long)sp * cp + c] = c < Cg ? src[(long long)c * S + sp] : (uint16_t)0;
         continue;
@@ -959,20 +1010,20 @@ __global__ void __launch_bounds__(256) pack_cl_kernel(const uint16_t* __restrict
   }
 }
 
-// As pack_cl_kernel for S % 8 == 0: one thread per 8 consecutive pixels and 8 channels.
+// As pack_cl for S % 8 == 0: one thread per 8 consecutive pixels and 8 channels.
 // Eight 16-byte loads (8 pixels of one channel plane each, coalesced across the warp), an
 // 8 x 8 transpose of 16-bit values in registers (byte permutes: pixel 2k takes the low
 // halves of word k of each channel pair, pixel 2k + 1 the high halves), eight 16-byte
 // stores (8 channels of one pixel each).
-__global__ void __launch_bounds__(256) pack_cl8_kernel(const uint16_t* __restrict__ x,
-                                                       uint16_t* __restrict__ xc, int N, int G,
-                                                       int Cg, int cp, int S) {
+__device__ __forceinline__ void pack_cl8(const uint16_t* __restrict__ x, uint16_t* __restrict__ xc,
+                                         int N, int G, int Cg, int cp, int S, int bx, int nx,
+                                         int by, int ny) {
   const int S8 = S / 8;
-  for (int gn = blockIdx.y; gn < G * N; gn += gridDim.y) {
+  for (int gn = by; gn < G * N; gn += ny) {
     const int gi = gn / N, n = gn - gi * N;
     const uint16_t* src = x + ((long long)n * G + gi) * Cg * (long long)S;
     uint16_t* dst = xc + (long long)gn * S * cp;
-    for (int j = blockIdx.x * 256 + threadIdx.x; j < S8; j += gridDim.x * 256) {
+    for (int j = bx * 256 + threadIdx.x; j < S8; j += nx * 256) {
       if (cp < 8) {
         // 2 or 4 channels per pixel: the same transpose, keeping the first cp channels
         uint32_t w[4][4];
@@ -1042,12 +1093,9 @@ __device__ __forceinline__ int prep_src(int k, int Cg, int KV, int cp, int block
   return (c < Cg && tap < KV) ? c * KV + tap : -1;
 }
 
-__global__ void __launch_bounds__(256) prep_weights_kernel(const uint16_t* __restrict__ w,
-                                                           uint16_t* __restrict__ wp, int M,
-                                                           int Cg, int KV, int kpad, int cp,
-                                                           int block64) {
-  extern __shared__ uint16_t row[];
-  const int m = blockIdx.x;
+__device__ __forceinline__ void prep_weights_row(const uint16_t* __restrict__ w, uint16_t* __restrict__ wp,
+                                                 int m, int Cg, int KV, int kpad, int cp, int block64,
+                                                 uint16_t* row) {
   const int Kg = Cg * KV;
   const uint16_t* src = w + (long long)m * Kg;
   if ((Kg % 8) == 0) {
@@ -1070,12 +1118,50 @@ __global__ void __launch_bounds__(256) prep_weights_kernel(const uint16_t* __res
   }
 }
 
+enum PackKind { kPackBlock64 = 0, kPackBlock64Scalar = 1, kPackCl8 = 2, kPackCl = 3 };
+
+struct PrologueArgs {
+  const uint16_t* w;
+  uint16_t* wp;         // weight copy, or null (no weight blocks)
+  int wblocks;          // = M when wp, else 0
+  int Cg, KV, kpad, cp, block64;
+  const uint16_t* x;
+  uint16_t* xp;
+  int kind;             // PackKind
+  int N, C, G;
+  long long S;
+  long long nx;         // pack blocks along the position axis
+  int ny;               // pack blocks along the channel-block / plane axis
+};
+
+__global__ void __launch_bounds__(256) prologue_kernel(const PrologueArgs p) {
+  extern __shared__ __align__(16) uint16_t psm[];
+  ptx::pdl_trigger();  // the main kernel may set itself up meanwhile
+  ptx::pdl_wait();     // X and W may be the previous kernel's outputs
+  long long b = blockIdx.x;
+  if (b < p.wblocks) {
+    prep_weights_row(p.w, p.wp, (int)b, p.Cg, p.KV, p.kpad, p.cp, p.block64, psm);
+    return;
+  }
+  b -= p.wblocks;
+  const long long bx = b % p.nx;
+  const int by = (int)(b / p.nx);
+  switch (p.kind) {
+    case kPackBlock64: pack_x_block(p.x, p.xp, p.N, p.C, p.S, bx, by, psm); break;
+    case kPackBlock64Scalar: pack_x_scalar(p.x, p.xp, p.N, p.C, p.S, bx, p.nx); break;
+    case kPackCl8: pack_cl8(p.x, p.xp, p.N, p.G, p.Cg, p.cp, (int)p.S, (int)bx, (int)p.nx, by, p.ny); break;
+    default: pack_cl(p.x, p.xp, p.N, p.G, p.Cg, p.cp, (int)p.S, (int)bx, (int)p.nx, by, p.ny); break;
+  }
+}
+
 // Y = act(sum_s partial[s] + B + Z), the splits added in order 0..S-1.
 template <int ACT>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const ConvGeom g, const float* part,
                                                             int splits, const __half* b,
                                                             const __half* z, __half* y,
                                                             long long total) {
+  ptx::pdl_wait();  // the partials are the previous kernel's output
+  ptx::pdl_trigger();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
     float acc = part[i];
@@ -1155,13 +1241,13 @@ template <int BN, bool SPLIT>
 int launch_t(const ConvGeom& g, const IgemmConfig& c, const TcArgs& ta, const CUtensorMap& tm,
              const CUtensorMap& ty, cudaStream_t s) {
   // the gather's in-flight depth is sized for this ring (no wait on a chunk it still owes)
-  if (c.stages <= gather_depth(BN)) return (int)cudaErrorInvalidValue;
+  if (c.stages < 2 * gather_depth(BN)) return (int)cudaErrorInvalidValue;
   const size_t smem = igemm_tc_smem_bytes(BN, c.stages);
   cudaError_t e = cudaFuncSetAttribute(igemm_tc_kernel<BN, SPLIT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  igemm_tc_kernel<BN, SPLIT><<<(unsigned)c.grid, kThreads, smem, s>>>(g, ta, tm, ty);
-  return (int)cudaGetLastError();
+  return launch_pdl(igemm_tc_kernel<BN, SPLIT>, dim3((unsigned)c.grid), dim3(kThreads), smem, s, g,
+                    ta, tm, ty);
 }
 
 template <bool SPLIT>
@@ -1185,8 +1271,8 @@ int launch_tma_t(const ConvGeom& g, const IgemmConfig& c, const TmaArgs& t, cons
   cudaError_t e = cudaFuncSetAttribute(igemm_tma_kernel<BN, SPLIT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  igemm_tma_kernel<BN, SPLIT><<<(unsigned)c.grid, kTmaThreads, smem, s>>>(g, t, tx, tw);
-  return (int)cudaGetLastError();
+  return launch_pdl(igemm_tma_kernel<BN, SPLIT>, dim3((unsigned)c.grid), dim3(kTmaThreads), smem,
+                    s, g, t, tx, tw);
 }
 
 int launch_reduce(const ConvGeom& g, const IgemmConfig& c, const float* part, const __half* b,
@@ -1194,11 +1280,13 @@ int launch_reduce(const ConvGeom& g, const IgemmConfig& c, const float* part, co
   const long long total = (long long)g.N * g.M * g.P;
   long long blocks = (total + 255) / 256;
   if (blocks > 152LL * 32) blocks = 152LL * 32;
-#define FCONV_REDUCE(ACT)                                                                    \
-  splitk_reduce_kernel<ACT><<<(unsigned)blocks, 256, 0, s>>>(g, part, c.split_k, b, z, y, total)
+  int err = 0;
+#define FCONV_REDUCE(ACT)                                                                  \
+  err = launch_pdl(splitk_reduce_kernel<ACT>, dim3((unsigned)blocks), dim3(256), 0, s, g, part, \
+                   c.split_k, b, z, y, total)
   FCONV_ACT_SWITCH(g.act, FCONV_REDUCE)
 #undef FCONV_REDUCE
-  return (int)cudaGetLastError();
+  return err;
 }
 
 }  // namespace
@@ -1244,8 +1332,8 @@ size_t igemm_tc_workspace_bytes(const ConvGeom& g, const IgemmConfig& c) {
 bool igemm_tc_tma_capable(const ConvGeom& g) { return tma_shape(g).ok; }
 
 int igemm_tc_launches(const ConvGeom& g, const IgemmConfig& c) {
-  const bool tma = use_tma(g, c.a_path);
-  return 2 + (needs_prep(g, tma) ? 1 : 0) + (c.split_k > 1 ? 1 : 0);
+  (void)g;
+  return 2 + (c.split_k > 1 ? 1 : 0);  // prologue, main kernel, split-K reduce
 }
 
 long long igemm_tc_mtiles(const ConvGeom& g, int a_path) {
@@ -1282,55 +1370,71 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
   EncodeTiledFn enc = encode_fn();
   if (!enc) return (int)cudaErrorNotSupported;
   const bool tma = use_tma(g, c.a_path);
-  const uint16_t* wmat = (const uint16_t*)a.w;
   uint8_t* ws = (uint8_t*)a.ws;
   const size_t pb = prep_bytes(g, tma);
   const int kpad = (int)kpad_of(g, tma);
   const int cp = cp_of(g);
-  if (pb) {
-    uint16_t* wp = (uint16_t*)ws;
-    const size_t rowbytes = (size_t)g.Kg * 2;
-    if (rowbytes > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(prep_weights_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)rowbytes);
-      if (e != cudaSuccess) return (int)e;
-    }
-    prep_weights_kernel<<<(unsigned)g.M, 256, rowbytes, s>>>((const uint16_t*)a.w, wp, g.M, g.Cg,
-                                                             g.KV, kpad, cp, tma ? 1 : 0);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return (int)e;
-    wmat = wp;
-  }
+  // one prologue launch: the weight copy (when the GEMM's K order is not W's) and X
+  // repacked for the A operand
   const size_t xb_bytes = pack_bytes(g, tma);
   uint16_t* xpack = (uint16_t*)(ws + pb);
-  if (tma) {
-    const long long S = g.IS;
-    const long long NS = (long long)g.N * S;
-    if (S % 8 == 0) {
-      dim3 pg((unsigned)((NS + 127) / 128), (unsigned)(g.C / 64), 1);
-      pack_x_kernel<<<pg, 256, 0, s>>>((const uint16_t*)a.x, xpack, g.N, g.C, S);
-    } else {
-      long long blocks = (NS * (g.C / 8) + 255) / 256;
-      if (blocks > 152LL * 32) blocks = 152LL * 32;
-      pack_x_scalar_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)a.x, xpack, g.N,
-                                                             g.C, S);
-    }
-  } else {
-    const long long planes = (long long)g.G * g.N;
-    const unsigned py = (unsigned)(planes < 65535 ? planes : 65535);
-    if (g.IS % 8 == 0) {
-      const dim3 pg((unsigned)((g.IS / 8 + 255) / 256), py, 1);
-      pack_cl8_kernel<<<pg, 256, 0, s>>>((const uint16_t*)a.x, xpack, g.N, g.G, g.Cg, cp, (int)g.IS);
-    } else {
-      const dim3 pg((unsigned)((g.IS + 255) / 256), py, 1);
-      pack_cl_kernel<<<pg, 256, 0, s>>>((const uint16_t*)a.x, xpack, g.N, g.G, g.Cg, cp, (int)g.IS);
-    }
-  }
   {
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return (int)e;
+    PrologueArgs pa;
+    pa.w = (const uint16_t*)a.w;
+    pa.wp = pb ? (uint16_t*)ws : nullptr;
+    pa.wblocks = pb ? g.M : 0;
+    pa.Cg = g.Cg;
+    pa.KV = g.KV;
+    pa.kpad = kpad;
+    pa.cp = cp;
+    pa.block64 = tma ? 1 : 0;
+    pa.x = (const uint16_t*)a.x;
+    pa.xp = xpack;
+    pa.N = g.N;
+    pa.C = g.C;
+    pa.G = g.G;
+    pa.S = g.IS;
+    size_t smem = pb ? (size_t)g.Kg * 2 : 0;
+    long long pack_blocks;
+    if (tma) {
+      const long long NS = (long long)g.N * g.IS;
+      if (g.IS % 8 == 0) {
+        pa.kind = kPackBlock64;
+        pa.nx = (NS + 127) / 128;
+        pa.ny = g.C / 64;
+        pack_blocks = pa.nx * pa.ny;
+        if (smem < kPackSmem) smem = kPackSmem;
+      } else {
+        pa.kind = kPackBlock64Scalar;
+        long long blocks = (NS * (g.C / 8) + 255) / 256;
+        if (blocks > 152LL * 32) blocks = 152LL * 32;
+        pa.nx = blocks;
+        pa.ny = 1;
+        pack_blocks = blocks;
+      }
+    } else {
+      const long long planes = (long long)g.G * g.N;
+      pa.ny = (int)(planes < 65535 ? planes : 65535);
+      if (g.IS % 8 == 0) {
+        pa.kind = kPackCl8;
+        pa.nx = (g.IS / 8 + 255) / 256;
+      } else {
+        pa.kind = kPackCl;
+        pa.nx = (g.IS + 255) / 256;
+      }
+      pack_blocks = pa.nx * pa.ny;
+    }
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(prologue_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return (int)e;
+    }
+    const long long blocks = pa.wblocks + pack_blocks;
+    if (blocks > 0x7fffffffLL) return (int)cudaErrorInvalidValue;
+    const int e = launch_pdl(prologue_kernel, dim3((unsigned)blocks), dim3(256), smem, s, pa);
+    if (e != 0) return e;
   }
+  const uint16_t* wmat = pb ? (const uint16_t*)ws : (const uint16_t*)a.w;
   const int wcols = pb ? kpad : g.Kg;
   CUtensorMap tm;
   std::memset(&tm, 0, sizeof(tm));

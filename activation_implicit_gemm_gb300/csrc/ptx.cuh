@@ -269,5 +269,14 @@ __device__ __forceinline__ void bulk_wait_read0() {
 // Waits until this thread's bulk stores are complete.
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream is still running:
+// pdl_wait() blocks until that kernel has completed and its memory is visible, so it must
+// come before the first global access; pdl_trigger() lets the next kernel start early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace ptx
 }  // namespace fconv
