@@ -100,7 +100,6 @@ struct TcArgs {
   int stages;
   int cp;               // channels per packed pixel: 2, 4 or C/group rounded up to 8
   int row_units;        // copies per GEMM row: KV (cp < 8, one tap each) or KV * cp / 8
-  int ytma;             // Y leaves by TMA stores of [16 channels][32 pixels] boxes
   int upc;              // copies per 64-wide chunk: 8 (16 bytes), 16 (8 bytes), 32 (4 bytes)
   int chunks;           // ceil(KV * cp / 64)
   int chunks_per_split;
@@ -111,11 +110,23 @@ struct TcArgs {
   FastDiv fd_split, fd_gnt, fd_ntiles, fd_P, fd_OW, fd_OH;  // unit and pixel decoding
 };
 
+// TMEM accumulators of the gathered-A kernel: as many BN-column buffers as fit in the 512
+// columns (at most 8), drained by `sets` groups of epilogue warps that take the tiles in
+// turn, so that several tiles are in the epilogue at once.
+template <int BN>
+struct AccPlan {
+  static constexpr uint32_t cols = BN < 32 ? 32 : BN;
+  static constexpr int nacc = (512 / cols) > 8 ? 8 : (int)(512 / cols);
+  static constexpr int sets = nacc >= 4 ? 4 : nacc;
+  static constexpr uint32_t tmem_cols = (uint32_t)nacc * cols;  // a power of two
+};
+constexpr int kMaxAcc = 8;
+
 struct SharedCtl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t acc_full[2];
-  uint64_t acc_empty[2];
+  uint64_t acc_full[kMaxAcc];
+  uint64_t acc_empty[kMaxAcc];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -190,8 +201,6 @@ struct EpiRows {
   long long obase;  // n * M * P + pixel index of this lane's pixel
   bool grp_ok;      // this lane's 8-pixel group exists
   long long gbase;  // n * M * P + first pixel of that group
-  bool run_ok;      // TMA-stored Y: the warp's 32-pixel run exists ...
-  int run_p, run_n; // ... and starts at pixel run_p of image run_n
 };
 
 // Z of channels mcb + lane / 4 and mcb + lane / 4 + 8 for this lane's pixel group.
@@ -237,8 +246,7 @@ template <int BN, int ACT>
 __device__ __forceinline__ void epilogue_tile(const ConvGeom& g, const __half* b, const __half* z,
                                               void* y, bool vec, const EpiRows& er, int m_first,
                                               int m_end, uint32_t acc, int c_first, int c_step,
-                                              int lane, __half* ys, uint4 zn0, uint4 zn1,
-                                              const CUtensorMap* ytm) {
+                                              int lane, __half* ys, uint4 zn0, uint4 zn1) {
   const bool hz = z != nullptr, hb = b != nullptr;
   __half* zs = ys;  // Z passes through the same tile: each lane reads back only its own column
 #pragma unroll 1
@@ -262,11 +270,6 @@ __device__ __forceinline__ void epilogue_tile(const ConvGeom& g, const __half* b
       if (vec && hz && c0 + c_step < BN) load_z16(z, er, mcb + c_step, m_end, g.P, lane, zn0, zn1);
       uint32_t bl = 0;  // bias of channel mcb + lane % 16, requested before the accumulator
       if (hb) bl = ptx::ld1_u16(b + mcb + (lane & 15), (lane & 15) < nvalid ? 1u : 0u);
-      if (ytm) {
-        // the previous group's box must be read out of the staging tile before reuse
-        if (lane == 0) ptx::bulk_wait_read0();
-        __syncwarp();
-      }
       if (hz) {
         if (vec) {
           reinterpret_cast<uint4*>(zs)[(lane >> 2) * 4 + (lane & 3)] = zc0;
@@ -291,16 +294,6 @@ __device__ __forceinline__ void epilogue_tile(const ConvGeom& g, const __half* b
         for (int jj = 0; jj < 16; ++jj) v[jj] += __half2float(zs[jj * 32 + lane]);
       }
       stage16<ACT>(v, ys, lane, g.alpha, g.beta);
-      if (ytm) {
-        // one TMA store of the [16 channels][32 pixels] box (16 channels inside the group)
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && er.run_ok) {
-          ptx::tma_store_3d(ytm, ptx::smem_addr(ys), er.run_p, mcb, er.run_n);
-          ptx::bulk_commit();
-        }
-        continue;
-      }
       __syncwarp();
       __half* yh = static_cast<__half*>(y);
       if (vec) {
@@ -324,11 +317,13 @@ __device__ __forceinline__ void epilogue_tile(const ConvGeom& g, const __half* b
 // q = n * P + pixel.
 template <int BN, int ACT>
 __device__ __forceinline__ void gather_epilogue(const ConvGeom& g, const TcArgs& a, SharedCtl& ctl,
-                                                uint32_t tmem, uint8_t* staging, int warp, int lane,
-                                                const CUtensorMap* tmap_y) {
-  constexpr uint32_t kAccCols = BN < 32 ? 32 : BN;
-  const int q4 = (warp - kEpiWarp0) & 3;               // TMEM lane quarter
-  const int c_first = ((warp - kEpiWarp0) >> 2) * 16;  // 16-column groups c_first + 64 k
+                                                uint32_t tmem, uint8_t* staging, int warp, int lane) {
+  using AP = AccPlan<BN>;
+  const int q4 = (warp - kEpiWarp0) & 3;  // TMEM lane quarter
+  const int j = (warp - kEpiWarp0) >> 2;
+  const int eset = j % AP::sets;          // takes tiles tcount = eset, eset + sets, ...
+  constexpr int kWpq = 4 / AP::sets;      // warps of a set per lane quarter
+  const int c_first = (j / AP::sets) * 16;  // 16-column groups c_first + 16 kWpq k
   const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
   // 16-byte Y/Z vectors need 8-pixel groups inside one image (P % 8 == 0)
   const bool vec = (g.P % 8) == 0;
@@ -336,11 +331,12 @@ __device__ __forceinline__ void gather_epilogue(const ConvGeom& g, const TcArgs&
   const long long NP = (long long)g.N * g.P;
   const long long MP = (long long)g.M * g.P;
   volatile int* abort_flag = &ctl.abort_flag;
-  uint32_t tcount = 0;
-  for (long long u = blockIdx.x; u < a.units; u += gridDim.x, ++tcount) {
+  uint32_t tcount = (uint32_t)eset;
+  for (long long u = blockIdx.x + (long long)eset * gridDim.x; u < a.units;
+       u += (long long)AP::sets * gridDim.x, tcount += AP::sets) {
     if (*abort_flag) break;
     const Unit un = decode_unit(u, a, g.G);
-    const uint32_t b = tcount & 1u;
+    const uint32_t b = tcount % (uint32_t)AP::nacc;
     EpiRows er;
     const long long q = un.rt * kBM + q4 * 32 + lane;
     er.row_ok = q < NP;
@@ -356,34 +352,27 @@ __device__ __forceinline__ void gather_epilogue(const ConvGeom& g, const TcArgs&
       const long long gn = fast_div((uint32_t)gq, a.fd_P);
       er.gbase = gn * MP + (gq - gn * g.P);
     }
-    const long long rq = un.rt * kBM + q4 * 32;
-    er.run_ok = rq < NP;
-    er.run_n = er.run_ok ? (int)fast_div((uint32_t)rq, a.fd_P) : 0;
-    er.run_p = (int)(rq - (long long)er.run_n * g.P);
     const int m_first = un.grp * g.Mg + un.ct * BN, m_end = un.grp * g.Mg + g.Mg;
     void* out = a.y;
     if constexpr (ACT == kActPartial) out = a.part + (long long)un.sp * NP * g.M;
     uint4 zn0 = make_uint4(0, 0, 0, 0), zn1 = zn0;
     if (ACT != kActPartial && vec && a.z && m_first + c_first < m_end)
       load_z16(a.z, er, m_first + c_first, m_end, g.P, lane, zn0, zn1);
-    if (!bounded_wait(ptx::smem_addr(&ctl.acc_full[b]), (tcount >> 1) & 1, abort_flag)) break;
+    if (!bounded_wait(ptx::smem_addr(&ctl.acc_full[b]), (tcount / AP::nacc) & 1, abort_flag)) break;
     ptx::tc_fence_after();
-    epilogue_tile<BN, ACT>(g, a.b, a.z, out, vec, er, m_first, m_end, lane_base + b * kAccCols,
-                           c_first, 4 * 16, lane, ys, zn0, zn1,
-                           (ACT != kActPartial && a.ytma) ? tmap_y : nullptr);
+    epilogue_tile<BN, ACT>(g, a.b, a.z, out, vec, er, m_first, m_end, lane_base + b * AP::cols,
+                           c_first, kWpq * 16, lane, ys, zn0, zn1);
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl.acc_empty[b]));
   }
-  if (a.ytma && lane == 0) ptx::bulk_wait0();  // Y stores complete before the CTA ends
 }
 
 template <int BN, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
-    igemm_tc_kernel(const ConvGeom g, const TcArgs a, const __grid_constant__ CUtensorMap tmap_w,
-                    const __grid_constant__ CUtensorMap tmap_y) {
-  constexpr uint32_t kAccCols = BN < 32 ? 32 : BN;
-  constexpr uint32_t kTmemCols = 2 * kAccCols;  // 64..512, a power of two
+    igemm_tc_kernel(const ConvGeom g, const TcArgs a, const __grid_constant__ CUtensorMap tmap_w) {
+  using AP = AccPlan<BN>;
+  constexpr uint32_t kTmemCols = AP::tmem_cols;
   constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB
   constexpr uint32_t kBBytes = BN * kBK * 2;
   constexpr uint32_t kStageBytes = kABytes + kBBytes;
@@ -421,9 +410,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(ptx::smem_addr(&ctl.full[s]), 4 + 1);  // 4 gather warps + TMA
       ptx::mbar_init(ptx::smem_addr(&ctl.empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < AP::nacc; ++b) {
       ptx::mbar_init(ptx::smem_addr(&ctl.acc_full[b]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl.acc_empty[b]), kEpiWarps);
+      ptx::mbar_init(ptx::smem_addr(&ctl.acc_empty[b]), kEpiWarps / AP::sets);
     }
     ptx::mbar_init(ptx::smem_addr(&ctl.drain), 1);
     ctl.abort_flag = 0;
@@ -608,12 +597,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (long long u = blockIdx.x; u < a.units; u += gridDim.x, ++tcount) {
         if (*abort_flag) break;
         const Unit un = decode_unit(u, a, g.G);
-        const uint32_t b = tcount & 1u;
-        if (tcount >= 2 &&
-            !bounded_wait(ptx::smem_addr(&ctl.acc_empty[b]), ((tcount >> 1) - 1) & 1, abort_flag))
+        const uint32_t b = tcount % (uint32_t)AP::nacc;
+        if (tcount >= (uint32_t)AP::nacc &&
+            !bounded_wait(ptx::smem_addr(&ctl.acc_empty[b]), ((tcount / AP::nacc) - 1) & 1, abort_flag))
           break;
         ptx::tc_fence_after();
-        const uint32_t dacc = tmem + b * kAccCols;
+        const uint32_t dacc = tmem + b * AP::cols;
         bool stop = false;
         for (int i = 0; i < un.nk; ++i, ++it) {
           const int s = (int)(it % (uint32_t)S);
@@ -641,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ================================================================ epilogue (warps 0-7)
     // one loop per activation, chosen once: the group loop carries no dispatch
-#define FCONV_EPI_LOOP(ACT) gather_epilogue<BN, ACT>(g, a, ctl, tmem, dsmem + (base - ptx::smem_addr(dsmem)) + (size_t)S * kStageBytes, warp, lane, &tmap_y)
+#define FCONV_EPI_LOOP(ACT) gather_epilogue<BN, ACT>(g, a, ctl, tmem, dsmem + (base - ptx::smem_addr(dsmem)) + (size_t)S * kStageBytes, warp, lane)
     if constexpr (SPLIT) {
       FCONV_EPI_LOOP(kActPartial);
     } else {
@@ -762,7 +751,7 @@ __device__ __forceinline__ void tma_epilogue(const ConvGeom& g, const TmaArgs& a
     if (!bounded_wait(ptx::smem_addr(&ctl.acc_full[b]), (tcount >> 1) & 1, abort_flag)) break;
     ptx::tc_fence_after();
     epilogue_tile<BN, ACT>(g, a.b, a.z, out, vec, er, m_first, m_end, lane_base + b * kAccCols,
-                           half * 16, 32, lane, ys, zn0, zn1, nullptr);
+                           half * 16, 32, lane, ys, zn0, zn1);
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl.acc_empty[b]));
@@ -910,10 +899,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 // prologue_kernel: its first `wblocks` blocks write the weight copy (one output channel
 // each), the others repack X. Both parts only move data.
 
-// X (N, C, spatial S) -> Xb[c/64][n][s][64]. Block (x, cb) moves 64 channels of the
-// flattened positions q = n*S + s in [128x, 128x + 128): four 16-byte loads per thread
-// (8 positions of one channel), all in flight, into a shared tile, then four 16-byte
-// stores per thread (8 channels of one position). Needs S % 8 == 0 (a load never
+// X (N, C, spatial S) -> Xb[c/64][n][s][64]. Block (x, cb), x = n * sblocks + sb, moves 64
+// channels of positions s in [128 sb, 128 sb + 128) of image n: four 16-byte loads per
+// thread (8 positions of one channel), all in flight, into a shared tile, then four
+// 16-byte stores per thread (8 channels of one position). Needs S % 8 == 0 (a load never
 // straddles two images); otherwise pack_x_scalar is used.
 constexpr int kPackPitch = 138;  // halves per channel row: 16-byte rows, few bank conflicts
 constexpr size_t kPackSmem = 64 * kPackPitch * 2;
@@ -922,18 +911,19 @@ __device__ __forceinline__ void pack_x_block(const uint16_t* __restrict__ x, uin
                                              int N, int C, long long S, long long bx, int cb,
                                              uint16_t* t) {
   const long long NS = (long long)N * S;
-  const long long q0 = bx * 128;
+  const uint32_t sblocks = (uint32_t)((S + 127) / 128);
+  const long long n = (uint32_t)bx / sblocks;  // block indices stay below 2^31
+  const long long s0 = (bx - n * sblocks) * 128;
+  const int rows = (int)min(128LL, S - s0);  // positions of this block (a multiple of 8)
+  const long long q0 = n * S + s0;
+  const uint16_t* src = x + (n * C + (long long)cb * 64) * S + s0;
   uint4 buf[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int v = threadIdx.x + 256 * i;
     const int c = v >> 4, pv = v & 15;
-    const long long q = q0 + pv * 8;
     buf[i] = make_uint4(0, 0, 0, 0);
-    if (q < NS) {
-      const long long n = q / S, sp = q - n * S;
-      buf[i] = *reinterpret_cast<const uint4*>(x + ((n * C + (long long)cb * 64 + c) * S + sp));
-    }
+    if (pv * 8 < rows) buf[i] = ptx::ldg_nc_v4(src + (long long)c * S + pv * 8);
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -948,7 +938,7 @@ __device__ __forceinline__ void pack_x_block(const uint16_t* __restrict__ x, uin
   for (int i = 0; i < 4; ++i) {
     const int o = threadIdx.x + 256 * i;
     const int p = o >> 3, part = o & 7;
-    if (q0 + p >= NS) continue;
+    if (p >= rows) continue;
     uint32_t w[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e)
@@ -1010,68 +1000,72 @@ __device__ __forceinline__ void pack_cl(const uint16_t* __restrict__ x, uint16_t
   }
 }
 
-// As pack_cl for S % 8 == 0: one thread per 8 consecutive pixels and 8 channels.
-// Eight 16-byte loads (8 pixels of one channel plane each, coalesced across the warp), an
-// 8 x 8 transpose of 16-bit values in registers (byte permutes: pixel 2k takes the low
-// halves of word k of each channel pair, pixel 2k + 1 the high halves), eight 16-byte
-// stores (8 channels of one pixel each).
+// As pack_cl for S % 8 == 0: one work item per (plane gn, 8-channel group, 8 consecutive
+// pixels j), items spread over the whole grid (item i of `items`, grid-stride from bi in
+// steps of nb). Eight 16-byte loads (8 pixels of one channel plane each, coalesced across
+// the warp), an 8 x 8 transpose of 16-bit values in registers (byte permutes: pixel 2k
+// takes the low halves of word k of each channel pair, pixel 2k + 1 the high halves), eight
+// 16-byte stores (8 channels of one pixel each).
 __device__ __forceinline__ void pack_cl8(const uint16_t* __restrict__ x, uint16_t* __restrict__ xc,
-                                         int N, int G, int Cg, int cp, int S, int bx, int nx,
-                                         int by, int ny) {
+                                         int N, int G, int Cg, int cp, int S, long long bi,
+                                         long long nb) {
   const int S8 = S / 8;
-  for (int gn = by; gn < G * N; gn += ny) {
+  const int groups = cp >= 8 ? cp / 8 : 1;
+  const long long items = (long long)G * N * groups * S8;
+  for (long long it = bi * 256 + threadIdx.x; it < items; it += nb * 256) {
+    // 32-bit decoding (the host keeps items below 2^31 on this path)
+    const uint32_t rest = (uint32_t)it / (uint32_t)S8;
+    const int j = (int)((uint32_t)it - rest * (uint32_t)S8);
+    const int c8 = (int)(rest % (uint32_t)groups) * 8;
+    const int gn = (int)(rest / (uint32_t)groups);
     const int gi = gn / N, n = gn - gi * N;
     const uint16_t* src = x + ((long long)n * G + gi) * Cg * (long long)S;
     uint16_t* dst = xc + (long long)gn * S * cp;
-    for (int j = bx * 256 + threadIdx.x; j < S8; j += nx * 256) {
-      if (cp < 8) {
-        // 2 or 4 channels per pixel: the same transpose, keeping the first cp channels
-        uint32_t w[4][4];
+    if (cp < 8) {
+      // 2 or 4 channels per pixel: the same transpose, keeping the first cp channels
+      uint32_t w[4][4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint4 r = make_uint4(0, 0, 0, 0);
-          if (c < Cg && c < cp) r = ptx::ldg_nc_v4(src + (long long)c * S + 8LL * j);
-          w[c][0] = r.x; w[c][1] = r.y; w[c][2] = r.z; w[c][3] = r.w;
-        }
-        // the thread's 8 pixels are 8 * cp contiguous elements: 16-byte stores
-        uint32_t a0[4], a1[4];
+      for (int c = 0; c < 4; ++c) {
+        uint4 r = make_uint4(0, 0, 0, 0);
+        if (c < Cg && c < cp) r = ptx::ldg_nc_v4(src + (long long)c * S + 8LL * j);
+        w[c][0] = r.x; w[c][1] = r.y; w[c][2] = r.z; w[c][3] = r.w;
+      }
+      // the item's 8 pixels are 8 * cp contiguous elements: 16-byte stores
+      uint32_t a0[4], a1[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        a0[k] = __byte_perm(w[0][k], w[1][k], 0x5410);  // pixel 2k, channels 0-1
+        a1[k] = __byte_perm(w[0][k], w[1][k], 0x7632);  // pixel 2k + 1
+      }
+      if (cp == 2) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          ptx::st_global_v4(dst + (8LL * j + 4 * h) * 2,
+                            make_uint4(a0[2 * h], a1[2 * h], a0[2 * h + 1], a1[2 * h + 1]));
+      } else {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          a0[k] = __byte_perm(w[0][k], w[1][k], 0x5410);  // pixel 2k, channels 0-1
-          a1[k] = __byte_perm(w[0][k], w[1][k], 0x7632);  // pixel 2k + 1
-        }
-        if (cp == 2) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            ptx::st_global_v4(dst + (8LL * j + 4 * h) * 2,
-                              make_uint4(a0[2 * h], a1[2 * h], a0[2 * h + 1], a1[2 * h + 1]));
-        } else {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t b0 = __byte_perm(w[2][k], w[3][k], 0x5410), b1 = __byte_perm(w[2][k], w[3][k], 0x7632);
-            ptx::st_global_v4(dst + (8LL * j + 2 * k) * 4, make_uint4(a0[k], b0, a1[k], b1));
-          }
-        }
-        continue;
-      }
-      for (int c8 = 0; c8 < cp; c8 += 8) {
-        uint32_t w[8][4];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4 r = make_uint4(0, 0, 0, 0);
-          if (c8 + c < Cg) r = ptx::ldg_nc_v4(src + (long long)(c8 + c) * S + 8LL * j);
-          w[c][0] = r.x; w[c][1] = r.y; w[c][2] = r.z; w[c][3] = r.w;
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint4 lo = make_uint4(__byte_perm(w[0][k], w[1][k], 0x5410), __byte_perm(w[2][k], w[3][k], 0x5410),
-                                      __byte_perm(w[4][k], w[5][k], 0x5410), __byte_perm(w[6][k], w[7][k], 0x5410));
-          const uint4 hi = make_uint4(__byte_perm(w[0][k], w[1][k], 0x7632), __byte_perm(w[2][k], w[3][k], 0x7632),
-                                      __byte_perm(w[4][k], w[5][k], 0x7632), __byte_perm(w[6][k], w[7][k], 0x7632));
-          ptx::st_global_v4(dst + (8LL * j + 2 * k) * cp + c8, lo);
-          ptx::st_global_v4(dst + (8LL * j + 2 * k + 1) * cp + c8, hi);
+          const uint32_t b0 = __byte_perm(w[2][k], w[3][k], 0x5410), b1 = __byte_perm(w[2][k], w[3][k], 0x7632);
+          ptx::st_global_v4(dst + (8LL * j + 2 * k) * 4, make_uint4(a0[k], b0, a1[k], b1));
         }
       }
+      continue;
+    }
+    uint32_t w[8][4];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint4 r = make_uint4(0, 0, 0, 0);
+      if (c8 + c < Cg) r = ptx::ldg_nc_v4(src + (long long)(c8 + c) * S + 8LL * j);
+      w[c][0] = r.x; w[c][1] = r.y; w[c][2] = r.z; w[c][3] = r.w;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 lo = make_uint4(__byte_perm(w[0][k], w[1][k], 0x5410), __byte_perm(w[2][k], w[3][k], 0x5410),
+                                  __byte_perm(w[4][k], w[5][k], 0x5410), __byte_perm(w[6][k], w[7][k], 0x5410));
+      const uint4 hi = make_uint4(__byte_perm(w[0][k], w[1][k], 0x7632), __byte_perm(w[2][k], w[3][k], 0x7632),
+                                  __byte_perm(w[4][k], w[5][k], 0x7632), __byte_perm(w[6][k], w[7][k], 0x7632));
+      ptx::st_global_v4(dst + (8LL * j + 2 * k) * cp + c8, lo);
+      ptx::st_global_v4(dst + (8LL * j + 2 * k + 1) * cp + c8, hi);
     }
   }
 }
@@ -1149,7 +1143,7 @@ __global__ void __launch_bounds__(256) prologue_kernel(const PrologueArgs p) {
   switch (p.kind) {
     case kPackBlock64: pack_x_block(p.x, p.xp, p.N, p.C, p.S, bx, by, psm); break;
     case kPackBlock64Scalar: pack_x_scalar(p.x, p.xp, p.N, p.C, p.S, bx, p.nx); break;
-    case kPackCl8: pack_cl8(p.x, p.xp, p.N, p.G, p.Cg, p.cp, (int)p.S, (int)bx, (int)p.nx, by, p.ny); break;
+    case kPackCl8: pack_cl8(p.x, p.xp, p.N, p.G, p.Cg, p.cp, (int)p.S, bx, p.nx); break;
     default: pack_cl(p.x, p.xp, p.N, p.G, p.Cg, p.cp, (int)p.S, (int)bx, (int)p.nx, by, p.ny); break;
   }
 }
@@ -1239,7 +1233,7 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 template <int BN, bool SPLIT>
 int launch_t(const ConvGeom& g, const IgemmConfig& c, const TcArgs& ta, const CUtensorMap& tm,
-             const CUtensorMap& ty, cudaStream_t s) {
+             cudaStream_t s) {
   // the gather's in-flight depth is sized for this ring (no wait on a chunk it still owes)
   if (c.stages < 2 * gather_depth(BN)) return (int)cudaErrorInvalidValue;
   const size_t smem = igemm_tc_smem_bytes(BN, c.stages);
@@ -1247,18 +1241,18 @@ int launch_t(const ConvGeom& g, const IgemmConfig& c, const TcArgs& ta, const CU
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
   return launch_pdl(igemm_tc_kernel<BN, SPLIT>, dim3((unsigned)c.grid), dim3(kThreads), smem, s, g,
-                    ta, tm, ty);
+                    ta, tm);
 }
 
 template <bool SPLIT>
 int launch_bn(const ConvGeom& g, const IgemmConfig& c, const TcArgs& ta, const CUtensorMap& tm,
-              const CUtensorMap& ty, cudaStream_t s) {
+              cudaStream_t s) {
   switch (c.tile_n) {
-    case 16: return launch_t<16, SPLIT>(g, c, ta, tm, ty, s);
-    case 32: return launch_t<32, SPLIT>(g, c, ta, tm, ty, s);
-    case 64: return launch_t<64, SPLIT>(g, c, ta, tm, ty, s);
-    case 128: return launch_t<128, SPLIT>(g, c, ta, tm, ty, s);
-    case 256: return launch_t<256, SPLIT>(g, c, ta, tm, ty, s);
+    case 16: return launch_t<16, SPLIT>(g, c, ta, tm, s);
+    case 32: return launch_t<32, SPLIT>(g, c, ta, tm, s);
+    case 64: return launch_t<64, SPLIT>(g, c, ta, tm, s);
+    case 128: return launch_t<128, SPLIT>(g, c, ta, tm, s);
+    case 256: return launch_t<256, SPLIT>(g, c, ta, tm, s);
     default: return (int)cudaErrorInvalidValue;
   }
 }
@@ -1400,7 +1394,7 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
       const long long NS = (long long)g.N * g.IS;
       if (g.IS % 8 == 0) {
         pa.kind = kPackBlock64;
-        pa.nx = (NS + 127) / 128;
+        pa.nx = (long long)g.N * ((g.IS + 127) / 128);
         pa.ny = g.C / 64;
         pack_blocks = pa.nx * pa.ny;
         if (smem < kPackSmem) smem = kPackSmem;
@@ -1415,9 +1409,14 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
     } else {
       const long long planes = (long long)g.G * g.N;
       pa.ny = (int)(planes < 65535 ? planes : 65535);
-      if (g.IS % 8 == 0) {
+      const long long items = planes * (cp >= 8 ? cp / 8 : 1) * (g.IS / 8);
+      if (g.IS % 8 == 0 && items + 152LL * 16 * 256 < 0x7fffffffLL) {
+        // one item per (plane, 8-channel group, 8 pixels); enough blocks to fill the GPU
         pa.kind = kPackCl8;
-        pa.nx = (g.IS / 8 + 255) / 256;
+        long long nb = (items + 255) / 256;
+        if (nb > 152LL * 16) nb = 152LL * 16;
+        pa.nx = nb;
+        pa.ny = 1;
       } else {
         pa.kind = kPackCl;
         pa.nx = (g.IS + 255) / 256;
@@ -1524,22 +1523,7 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
   ta.fd_OW = make_fastdiv((uint32_t)g.OW);
   ta.fd_OH = make_fastdiv((uint32_t)g.OH);
   ta.fd_ntiles = make_fastdiv((uint32_t)ta.ntiles);
-  // Y by TMA stores: 32-pixel runs inside one image (P % 32 == 0), 16-channel boxes inside one
-  // group (C_out/group % 16 == 0); split-K partials go through the plain stores
-  CUtensorMap ty;
-  std::memset(&ty, 0, sizeof(ty));
-  ta.ytma = (c.split_k <= 1 && g.P % 32 == 0 && g.Mg % 16 == 0) ? 1 : 0;
-  if (ta.ytma) {
-    cuuint64_t ydims[3] = {(cuuint64_t)g.P, (cuuint64_t)g.M, (cuuint64_t)g.N};
-    cuuint64_t ystr[2] = {(cuuint64_t)g.P * 2, (cuuint64_t)g.M * g.P * 2};
-    cuuint32_t ybox[3] = {32, 16, 1};
-    cuuint32_t yes[3] = {1, 1, 1};
-    cr = enc(&ty, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, (void*)a.y, ydims, ystr, ybox, yes,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr != CUDA_SUCCESS) ta.ytma = 0;
-  }
-  const int err = c.split_k > 1 ? launch_bn<true>(g, c, ta, tm, ty, s) : launch_bn<false>(g, c, ta, tm, ty, s);
+  const int err = c.split_k > 1 ? launch_bn<true>(g, c, ta, tm, s) : launch_bn<false>(g, c, ta, tm, s);
   if (err != 0 || c.split_k <= 1) return err;
   return launch_reduce(g, c, part, ta.b, ta.z, ta.y, s);
 }
