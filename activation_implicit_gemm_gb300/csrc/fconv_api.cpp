@@ -186,8 +186,9 @@ void plan_igemm(fconv_plan* p, const fconv_options* o) {
   int split = 1;
   if (o && o->split_k > 0) {
     split = o->split_k;
-  } else if (tiles * 2 <= p->sms && chunks >= 2) {
-    // one persistent CTA per SM: split K only when at least two splits fit per tile
+  } else if (tiles * 2 <= p->sms && chunks >= 8) {
+    // one persistent CTA per SM: split K only when at least two splits fit per tile and K
+    // is long enough (8+ chunks) for the partials' round trip and the reduce launch to pay
     long long s = p->sms / tiles;
     if (s > chunks) s = chunks;
     if (s > 16) s = 16;

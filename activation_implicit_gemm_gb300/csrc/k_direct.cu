@@ -41,13 +41,28 @@ __global__ void __launch_bounds__(256) direct_conv_kernel(ConvGeom g, const T* _
   }
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
-    const long long o = idx % g.P;
-    const long long nm = idx / g.P;
-    const int m = (int)(nm % g.M);
-    const int n = (int)(nm / g.M);
-    const int ow = (int)(o % g.OW);
-    const int oh = (int)((o / g.OW) % g.OH);
-    const int od = (int)(o / ((long long)g.OW * g.OH));
+    long long o;
+    int m, n, ow, oh, od;
+    if (total < 0x7fffffffLL) {  // 32-bit index decoding (the common case)
+      const uint32_t i32 = (uint32_t)idx, P32 = (uint32_t)g.P;
+      const uint32_t nm = i32 / P32, o32 = i32 - nm * P32;
+      m = (int)(nm % (uint32_t)g.M);
+      n = (int)(nm / (uint32_t)g.M);
+      const uint32_t t = o32 / (uint32_t)g.OW;
+      ow = (int)(o32 - t * (uint32_t)g.OW);
+      oh = (int)(t % (uint32_t)g.OH);
+      od = (int)(t / (uint32_t)g.OH);
+      o = o32;
+    } else {
+      o = idx % g.P;
+      const long long nm = idx / g.P;
+      m = (int)(nm % g.M);
+      n = (int)(nm / g.M);
+      ow = (int)(o % g.OW);
+      oh = (int)((o / g.OW) % g.OH);
+      od = (int)(o / ((long long)g.OW * g.OH));
+    }
+    (void)o;
     const int grp = m / g.Mg;
     const int iz0 = od * g.sD - g.pD, iy0 = oh * g.sH - g.pH, ix0 = ow * g.sW - g.pW;
     // the taps that land inside X, per axis (no test in the inner loops)

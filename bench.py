@@ -127,6 +127,14 @@ def bound_of(flops, bytes_, peaks):
     return "tensor" if flops / bytes_ >= ridge else "hbm"
 
 
+def main_kernel_name(case, route):
+    """The kernel that does the conv's arithmetic (the TMA-fed implicit GEMM takes
+    C/group a multiple of 64; other tensor-core convs gather their A operand)."""
+    if route == "igemm_tc":
+        return "igemm_tma_kernel" if case.w_shape[1] % 64 == 0 else "igemm_tc_kernel"
+    return {"depthwise": "dw_kernel_persistent", "direct": "direct_conv_kernel"}[route]
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -249,8 +257,7 @@ def run_ours(args):
     traffic = load_traffic(convs[top]["case"].name)
     roofline = {"bound": tb, "achieved": round(ach, 3), "peak": pk, "unit": unit,
                 "frac": round(ach / pk, 4), "traffic": traffic,
-                "kernel": {"igemm_tc": "igemm_tc_kernel", "depthwise": "dw_kernel_persistent",
-                           "direct": "direct_conv_kernel"}[tp.route],
+                "kernel": main_kernel_name(convs[top]["case"], tp.route),
                 "launch": convs[top]["case"].name, "peak_kind": f"{peaks_kind} (burst)",
                 "algorithmic_flops_per_launch": tp.flops,
                 "algorithmic_bytes_per_launch": tp.bytes}

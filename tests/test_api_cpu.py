@@ -147,13 +147,17 @@ def test_config_shapes_and_routes(lib):
 
 
 def test_split_k_planned_for_small_grids(lib):
-    # the 1-D config has 32 row tiles << 152 SMs: K is split; the big 2-D conv is not
+    # one row tile << 152 SMs and a long K (2304 = 36 chunks of 64): K is split
+    p = FusedConvPlan(_lib.F16, (1, 256, 8, 8), (128, 256, 3, 3), has_bias=True, has_z=True,
+                      pads=[1, 1, 1, 1])
+    assert p.split_k > 1
+    # f32 partials per split, plus the weights copied into the GEMM's K order
+    y_elems = np.prod(p.y_shape)
+    assert p.workspace_bytes >= p.split_k * 4 * y_elems + 2 * 128 * 256 * 9
+    # the 1-D config has 32 row tiles but only 5 chunks of K: too short to split
     c2 = workloads.case_by_name("1d_f16_64to64_k5_d2_same_upper_leakyrelu")
     p = FusedConvPlan(_lib.F16, c2.x_shape, c2.w_shape, has_bias=True, has_z=True, **c2.attrs())
-    assert p.split_k > 1
-    # f32 partials per split, plus the weights copied into the channel-inner K order
-    assert p.workspace_bytes >= p.split_k * 4 * np.prod(p.y_shape)
-    assert p.workspace_bytes - p.split_k * 4 * np.prod(p.y_shape) >= 2 * np.prod(c2.w_shape)
+    assert p.split_k == 1
     cb = workloads.case_by_name("cnn_b_64to128_16x16_z")
     p = FusedConvPlan(_lib.F16, cb.x_shape, cb.w_shape, has_z=True, **cb.attrs())
     # no split: the workspace holds the reordered weights and X repacked in 64-channel
