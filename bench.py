@@ -55,6 +55,26 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest `value` over all ranks of the initialised process group (a job takes as
+    long as its slowest rank). NCCL reduces a tensor on `device`, other backends on the
+    host; with one rank (or no process group) the value itself."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    on = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=on)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_step: float, ranks: int, steps: int, ms: float) -> float:
+    """Whole-job throughput of `ranks` replicas that each ran `steps` steps of
+    `flops_per_step` in `ms` milliseconds (the slowest rank's time)."""
+    return flops_per_step * ranks * steps / (ms * 1e-3) / 1e12
+
+
 class ClockSampler:
     """nvidia-smi SM clock / throttle-reason samples with host timestamps."""
 
@@ -219,13 +239,9 @@ def run_ours(args):
             per_conv_ms[i] += dt_ms
             s += dt_ms
         step_ms.append(s)
-    dev_ms = sum(step_ms)
-    if ws_n > 1:
-        tt = torch.tensor([dev_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        dev_ms = float(tt.item())
+    dev_ms = max_over_ranks(sum(step_ms), dev)
     ms_per_step = dev_ms / K
-    value = total_flops * ws_n * K / (dev_ms * 1e-3) / 1e12
+    value = job_tflops(total_flops, ws_n, K, dev_ms)
 
     # per-conv breakdown and the dominant launch's roofline
     per = []
@@ -287,12 +303,8 @@ def run_ours(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if ws_n > 1:
-        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = total_flops * ws_n * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    e2e_value = job_tflops(total_flops, ws_n, e2e_steps, e2e_ms)
 
     out = {"metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws_n,
            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
