@@ -94,17 +94,8 @@ __device__ __forceinline__ void store_block4(const float (&acc)[4][4], const T* 
             from_f32<T>(act_eval<ACT, sizeof(T) == 2>(acc[r][j] + zv[r][j], alpha, beta));
 }
 
-// Four consecutive elements starting at p (p 4-element aligned): one 8-byte (f16) or
-// 16-byte (f32) access.
-__device__ __forceinline__ void load4(const __half* p, float (&v)[4]) {
-  const uint2 r = *reinterpret_cast<const uint2*>(p);
-  const __half2 a = *reinterpret_cast<const __half2*>(&r.x), b = *reinterpret_cast<const __half2*>(&r.y);
-  v[0] = __low2float(a); v[1] = __high2float(a); v[2] = __low2float(b); v[3] = __high2float(b);
-}
-__device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
-  const float4 r = *reinterpret_cast<const float4*>(p);
-  v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w;
-}
+// Four consecutive outputs starting at p (p 4-element aligned): one 8-byte (f16) or
+// 16-byte (f32) store.
 __device__ __forceinline__ void store4(__half* p, const float (&v)[4]) {
   const __half2 a = __floats2half2_rn(v[0], v[1]), b = __floats2half2_rn(v[2], v[3]);
   uint2 r;

@@ -14,22 +14,25 @@
 // channels of one tap, so its validity is one test and its addresses one stride apart;
 // with C/group a multiple of 64 it uses (64-channel block, tap, channel), so that all
 // taps of a block reuse the same slab of X from L1.
-// The weights are then read from a copy in that order (prep_weights_kernel, into the
-// workspace); otherwise k = ci*KV + tap, W's own order.
+// The weights are then read from a copy in that order, written into the workspace by the
+// prologue launch, which also repacks X (channels innermost) for the A operand.
 //
-// Persistent, warp-specialised CTA (one per SM), 14 warps:
-//   warps 0-3   epilogue: tcgen05.ld of an accumulator (lane = pixel, column = channel),
-//               + B[m] + Z, activation, one rounding to f16, NC(D)HW store;
-//   warps 4-11  A gather, two sets of four warps taking alternate K chunks; thread t of a
-//               set owns tile row t (one output pixel), loads its 64 k values of the chunk
-//               (64 loads in flight) and writes them as eight 16-byte pieces into the
-//               128-byte-swizzled K-major layout the MMA descriptor reads;
-//   warp 12     allocates TMEM (two accumulators of BN f32 columns, so the epilogue of
-//               one tile overlaps the main loop of the next) and one lane issues
-//               tcgen05.mma (K = 16 each) and tcgen05.commit;
-//   warp 13     one lane streams the weight tiles with TMA (zero fill past the edges).
-// A ring of `stages` shared-memory chunks (A 16 KB + B BN*128 B each) with full/empty
-// mbarriers connects gather/TMA -> MMA; acc_full/acc_empty connect MMA <-> epilogue.
+// Two persistent, warp-specialised kernels (one CTA per SM) share the MMA and epilogue
+// design; they differ in how A reaches shared memory:
+//   igemm_tma_kernel (C/group % 64 == 0): A is one 5-D TMA box of X repacked in 64-channel
+//     blocks per chunk (TMA applies stride, dilation and zero padding); 10 warps: 8
+//     epilogue, MMA, TMA producer.
+//   igemm_tc_kernel (other C/group): A is gathered from a channels-last copy of X by two
+//     sets of four gather warps that take alternate chunks (thread t of a set owns tile
+//     row t, one output pixel, and issues one cp.async per valid 16/8/4-byte unit straight
+//     into the 128-byte-swizzled K-major row); 26 warps: 16 epilogue, 8 gather, MMA, TMA
+//     (weights).
+// One lane of the MMA warp issues tcgen05.mma (M = 128, N = BN, K = 16) and tcgen05.commit
+// into TMEM accumulators; the epilogue warps read them with tcgen05.ld (lane = pixel,
+// column = channel), add B[m] and Z, apply the activation, round once to f16 and store
+// NC(D)HW Y as 16-byte vectors through a per-warp staging tile. A ring of `stages`
+// shared-memory chunks (A 16 KB + B BN*128 B each) with full/empty mbarriers connects the
+// producers to the MMA; acc_full/acc_empty connect the MMA to the epilogue.
 //
 // Split-K (README variants implicit_im2col_tiled_reg_splitk: the reduction is
 // partitioned when the unsplit grid is too small, raw partial sums are combined, and
@@ -899,11 +902,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 // prologue_kernel: its first `wblocks` blocks write the weight copy (one output channel
 // each), the others repack X. Both parts only move data.
 
-// X (N, C, spatial S) -> Xb[c/64][n][s][64]. Block (x, cb), x = n * sblocks + sb, moves 64
-// channels of positions s in [128 sb, 128 sb + 128) of image n: four 16-byte loads per
-// thread (8 positions of one channel), all in flight, into a shared tile, then four
-// 16-byte stores per thread (8 channels of one position). Needs S % 8 == 0 (a load never
-// straddles two images); otherwise pack_x_scalar is used.
+// X (N, C, spatial S) -> Xb[c/64][n][s][64]. Block (x, cb) moves 64 channels of the
+// flattened positions q = n*S + s in [128x, 128x + 128), across image boundaries when S is
+// small: four 16-byte loads per thread (8 positions of one channel), all in flight, into a
+// shared tile, then four 16-byte stores per thread (8 channels of one position). Needs
+// S % 8 == 0 (a load never straddles two images) and N*S < 2^31 (32-bit position
+// decoding); otherwise pack_x_scalar is used.
 constexpr int kPackPitch = 138;  // halves per channel row: 16-byte rows, few bank conflicts
 constexpr size_t kPackSmem = 64 * kPackPitch * 2;
 
@@ -911,19 +915,19 @@ __device__ __forceinline__ void pack_x_block(const uint16_t* __restrict__ x, uin
                                              int N, int C, long long S, long long bx, int cb,
                                              uint16_t* t) {
   const long long NS = (long long)N * S;
-  const uint32_t sblocks = (uint32_t)((S + 127) / 128);
-  const long long n = (uint32_t)bx / sblocks;  // block indices stay below 2^31
-  const long long s0 = (bx - n * sblocks) * 128;
-  const int rows = (int)min(128LL, S - s0);  // positions of this block (a multiple of 8)
-  const long long q0 = n * S + s0;
-  const uint16_t* src = x + (n * C + (long long)cb * 64) * S + s0;
+  const long long q0 = bx * 128;
+  const int rows = (int)min(128LL, NS - q0);  // positions of this block (a multiple of 8)
   uint4 buf[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int v = threadIdx.x + 256 * i;
     const int c = v >> 4, pv = v & 15;
     buf[i] = make_uint4(0, 0, 0, 0);
-    if (pv * 8 < rows) buf[i] = ptx::ldg_nc_v4(src + (long long)c * S + pv * 8);
+    if (pv * 8 < rows) {
+      const uint32_t q = (uint32_t)(q0 + pv * 8);
+      const uint32_t n = q / (uint32_t)S, sp = q - n * (uint32_t)S;
+      buf[i] = ptx::ldg_nc_v4(x + (((long long)n * C + (long long)cb * 64 + c) * S + sp));
+    }
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -1392,9 +1396,9 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
     long long pack_blocks;
     if (tma) {
       const long long NS = (long long)g.N * g.IS;
-      if (g.IS % 8 == 0) {
+      if (g.IS % 8 == 0 && NS < 0x7fffff00LL) {
         pa.kind = kPackBlock64;
-        pa.nx = (long long)g.N * ((g.IS + 127) / 128);
+        pa.nx = (NS + 127) / 128;
         pa.ny = g.C / 64;
         pack_blocks = pa.nx * pa.ny;
         if (smem < kPackSmem) smem = kPackSmem;

@@ -253,22 +253,6 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tmap, int 
       : "memory");
 }
 
-// TMA store of a 3-D box from shared memory (bulk-group completion). Coordinates past the
-// tensor's extent are not written.
-__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-                   (uint64_t)tmap),
-               "r"(src), "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Waits until this thread's bulk stores have finished reading their shared-memory source.
-__device__ __forceinline__ void bulk_wait_read0() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// Waits until this thread's bulk stores are complete.
-__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 // Programmatic dependent launch. A kernel launched with programmatic stream
 // serialization may start while the previous kernel in the stream is still running:
 // pdl_wait() blocks until that kernel has completed and its memory is visible, so it must
