@@ -160,6 +160,11 @@ TC_CASES = [
                                          activation="Gelu"), True, False),
     ((2, 16, 12, 12), (32, 16, 2, 2), dict(strides=[2, 2]), False, False),
     ((2, 4, 9, 9), (4, 2, 3, 3), dict(group=2, auto_pad="VALID"), True, True),
+    # K in one chunk with 4-channel copy units (padding units zeroed once), ragged rows
+    ((3, 3, 11, 13), (10, 3, 3, 3), dict(pads=[1, 1, 1, 1], activation="QuickGelu"), False,
+     True),
+    # 4x4 images: one repack block spans five images (64-channel blocks, TMA-fed A)
+    ((5, 64, 4, 4), (48, 64, 3, 3), dict(pads=[1, 1, 1, 1]), True, True),
 ]
 
 
