@@ -161,16 +161,19 @@ fconv_status fconv_plan_output_shape(const fconv_plan* plan, int64_t y_shape[5],
 /* Applied begin/end pads per (depth, height, width) axis; missing axes read 0. */
 fconv_status fconv_plan_pads(const fconv_plan* plan, int64_t pad_begin[3], int64_t pad_end[3]);
 
-/* Device workspace bytes fconv_run needs (0 unless the plan splits K). */
+/* Device workspace bytes fconv_run needs. On the tensor-core route: the weights copied
+ * into the GEMM's K order (unless W is already in it), X repacked with channels innermost
+ * for the A operand, and the f32 partial sums of a split-K plan; 0 on the direct and
+ * depthwise routes. */
 fconv_status fconv_plan_workspace_size(const fconv_plan* plan, size_t* bytes);
 
 /* Route, tile and split chosen by the plan. */
 fconv_status fconv_plan_route(const fconv_plan* plan, fconv_route* route, int* tile_n,
                               int* split_k);
 
-/* Number of kernels one fconv_run of this plan launches (the convolution itself plus,
- * on the tensor-core route, the weight reordering, the X repacking for the TMA-fed A
- * operand and the split-K reduction, when the plan uses them). */
+/* Number of kernels one fconv_run of this plan launches: one on the direct and depthwise
+ * routes; on the tensor-core route a prologue (weight copy and X repack in one launch),
+ * the implicit GEMM and, when K is split, the reduction of the partial sums. */
 fconv_status fconv_plan_launches(const fconv_plan* plan, int* kernels);
 
 /* Algorithmic work of one fconv_run: 2 * N * P * M * (C/group) * prod(kernel) flops and
@@ -194,8 +197,9 @@ fconv_status fconv_check_device(void* stream);
  * cudaMalloc is unavailable or forbidden (inside a capture or allocator hook that must
  * not allocate, a host callback, a plugin whose host application owns every device
  * allocation, or a real-time path with a no-allocation rule). It takes the same
- * arguments as fconv_run minus the workspace: the scratch that a split-K plan needs
- * (fconv_plan_workspace_size) comes from a fixed array of FCONV_NOALLOC_SCRATCH_BYTES
+ * arguments as fconv_run minus the workspace: the workspace the plan needs
+ * (fconv_plan_workspace_size: the weight copy, the repacked X and any split-K partial
+ * sums of the tensor-core route) comes from a fixed array of FCONV_NOALLOC_SCRATCH_BYTES
  * compiled into the library, which every GPU that loads the library keeps until the
  * process exits. The pages this library follows have no counterpart of this call.
  *  - A plan needing more scratch than FCONV_NOALLOC_SCRATCH_BYTES is rejected with
