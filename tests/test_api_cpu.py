@@ -234,3 +234,26 @@ def test_invariant_divisor_arithmetic(lib):
     """The multiply-shift division the kernels use for index decoding agrees with
     ordinary integer division (checked by the library's host code)."""
     assert lib.fconv_selftest_fastdiv() == 0
+
+
+def test_launch_counts_and_workspace_regions(lib):
+    # tensor-core route: a prologue launch (weight copy + X repack) and the implicit GEMM,
+    # plus the reduction when K is split; the workspace holds exactly those buffers
+    ca = workloads.case_by_name("cnn_a_3to64_32x32")
+    p = FusedConvPlan(_lib.F16, ca.x_shape, ca.w_shape, **ca.attrs())
+    assert p.route == "igemm_tc" and p.split_k == 1 and p.launches == 2
+    # gathered A: X channels-last with 3 channels padded to 4; weights in (tap, channel)
+    # order, 9 taps x 4 channels padded to a multiple of 8 columns
+    wcopy = (2 * 64 * 40 + 1023) // 1024 * 1024
+    xcopy = (2 * 512 * 32 * 32 * 4 + 1023) // 1024 * 1024
+    assert p.workspace_bytes == wcopy + xcopy
+    ps = FusedConvPlan(_lib.F16, (1, 256, 8, 8), (128, 256, 3, 3), pads=[1, 1, 1, 1])
+    assert ps.split_k > 1 and ps.launches == 3
+    # one kernel and no workspace on the depthwise and direct routes
+    cd = workloads.case_by_name("stem_dw_128_k7")
+    pd = FusedConvPlan(_lib.F16, cd.x_shape, cd.w_shape, has_bias=True, has_z=True,
+                       **cd.attrs())
+    assert pd.route == "depthwise" and pd.launches == 1 and pd.workspace_bytes == 0
+    c1 = workloads.case_by_name("2d_f32_3to8_k3_relu")
+    p1 = FusedConvPlan(_lib.F32, c1.x_shape, c1.w_shape, has_bias=True, **c1.attrs())
+    assert p1.route == "direct" and p1.launches == 1 and p1.workspace_bytes == 0
