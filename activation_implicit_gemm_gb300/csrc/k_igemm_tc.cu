@@ -631,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bounded_wait(ptx::smem_addr(&ctl.drain), 0, abort_flag);
     }
   } else {
-    // ================================================================ epilogue (warps 0-7)
+    // ================================================================ epilogue (warps 0-15)
     // one loop per activation, chosen once: the group loop carries no dispatch
 #define FCONV_EPI_LOOP(ACT) gather_epilogue<BN, ACT>(g, a, ctl, tmem, dsmem + (base - ptx::smem_addr(dsmem)) + (size_t)S * kStageBytes, warp, lane)
     if constexpr (SPLIT) {
@@ -655,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ============================================================================
 // TMA-fed variant (C/group a multiple of 64). X is first repacked into blocks of 64
-// channels, channels innermost: Xb[c/64][n][d][h][w][64] (pack_x_kernel). A tile of
+// channels, channels innermost: Xb[c/64][n][d][h][w][64] (prologue launch). A tile of
 // output pixels is a box (Nb images x Dt x Ht x Wt, at most 128 pixels); for a chunk
 // (64-channel block cb, tap t) its A operand is one 5-D TMA box of Xb at
 // (0, ow0*sW - pW + kx*dW, oh0*sH - pH + ky*dH, od0*sD - pD + kz*dD, (g*Cg/64 + cb)*N + n0)

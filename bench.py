@@ -368,13 +368,41 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def strip_comments(src: str) -> str:
+    """C/C++/CUDA source without its comments and blank lines (string and character
+    literals kept), so that editing a comment does not count as changing a kernel."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = [ln.rstrip() for ln in "".join(out).split("\n")]
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
 def kernel_sources_digest():
+    """Digest of the library's code (comments excluded): the committed DRAM counters are
+    reported only for the code they were measured on."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "activation_implicit_gemm_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h", ".cpp")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+            h.update(f.encode() + b"\0")
+            h.update(strip_comments(open(os.path.join(csrc, f)).read()).encode())
     return h.hexdigest()[:16]
 
 
