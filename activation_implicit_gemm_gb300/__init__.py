@@ -55,7 +55,7 @@ class FusedConvPlan:
                  dilations=None, pads=None, auto_pad: str = "NOTSET", kernel_shape=None,
                  activation: Optional[str] = None, activation_params=None, device: int = -1,
                  route: str = "auto", split_k: int = 0, tile_n: int = 0, z_shape=None,
-                 a_path: str = "auto"):
+                 a_path: str = "auto", max_ctas: int = 0):
         lib = _lib.load()
         self._lib = lib
         self._ptr = ctypes.c_void_p()
@@ -86,7 +86,7 @@ class FusedConvPlan:
                               kernel_shape=kernel_shape, activation=activation,
                               activation_params=activation_params)
         opts = _lib.FconvOptions(ROUTES[route], int(split_k), int(tile_n),
-                                 {"auto": 0, "gather": 1, "tma": 2}[a_path])
+                                 {"auto": 0, "gather": 1, "tma": 2}[a_path], int(max_ctas))
         _check(lib.fconv_plan_create_ex(ctypes.byref(desc), device, ctypes.byref(opts),
                                         ctypes.byref(self._ptr)), "fconv_plan_create")
         ys = (ctypes.c_int64 * 5)()
@@ -174,12 +174,13 @@ def plan_for(x, w, b=None, z=None, **attrs) -> FusedConvPlan:
 def fused_conv(x, w, b=None, z=None, *, group: int = 1, strides=None, dilations=None,
                pads=None, auto_pad: str = "NOTSET", kernel_shape=None,
                activation: Optional[str] = None, activation_params=None, out=None,
-               route: str = "auto", split_k: int = 0, tile_n: int = 0, a_path: str = "auto"):
+               route: str = "auto", split_k: int = 0, tile_n: int = 0, a_path: str = "auto",
+               max_ctas: int = 0):
     """Y = act(conv(X, W) + B + Z) on CUDA tensors (the operator's ONNX-style attributes)."""
     if not x.is_cuda:
         raise ValueError("fused_conv runs on CUDA tensors only")
     p = plan_for(x, w, b, z, group=group, strides=strides, dilations=dilations, pads=pads,
                  auto_pad=auto_pad, kernel_shape=kernel_shape, activation=activation,
                  activation_params=activation_params, route=route, split_k=split_k,
-                 tile_n=tile_n, a_path=a_path)
+                 tile_n=tile_n, a_path=a_path, max_ctas=max_ctas)
     return p.run(x, w, b, z, y=out)

@@ -39,7 +39,7 @@ class FconvDesc(ctypes.Structure):
 
 class FconvOptions(ctypes.Structure):
     _fields_ = [("route", ctypes.c_int), ("split_k", ctypes.c_int), ("tile_n", ctypes.c_int),
-                ("a_path", ctypes.c_int)]
+                ("a_path", ctypes.c_int), ("max_ctas", ctypes.c_int)]
 
 
 EXPORTS = ["fconv_plan_create", "fconv_plan_create_ex", "fconv_plan_output_shape",

@@ -202,6 +202,7 @@ void plan_igemm(fconv_plan* p, const fconv_options* o) {
   c.split_k = split;
   const long long units = tiles * split;
   c.grid = units < p->sms ? units : p->sms;
+  if (g.max_ctas > 0 && c.grid > g.max_ctas) c.grid = g.max_ctas;
   p->workspace = igemm_tc_workspace_bytes(g, c);
 }
 
@@ -219,6 +220,11 @@ fconv_status create(const fconv_desc* d, int device, const fconv_options* o, fco
     return st;
   }
   p->sms = device_sms(device);
+  if (o && o->max_ctas < 0) {
+    delete p;
+    return FCONV_E_UNSUPPORTED;
+  }
+  p->g.max_ctas = o ? o->max_ctas : 0;
   const fconv_route want = o ? o->route : FCONV_ROUTE_AUTO;
   fconv_route route = want;
   if (want == FCONV_ROUTE_AUTO) {

@@ -30,6 +30,7 @@ struct ConvGeom {
   long long IS;                 // ID*IH*IW
   int KV;                       // KD*KH*KW
   int Kg;                       // Cg*KV
+  int max_ctas;                 // cap on persistent CTAs (0 = none)
 };
 
 struct ConvArgs {

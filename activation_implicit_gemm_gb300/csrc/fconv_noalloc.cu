@@ -1,10 +1,11 @@
 // fconv_run_noalloc: fconv_run for callers that cannot allocate device memory.
 //
-// The split-K scratch that fconv_run takes from the caller's workspace comes here from
-// one fixed, file-scope device array. Host code never uses the array's name as an
-// address (on the host it is only a stand-in symbol): the device address is looked up
-// once per device with cudaGetSymbolAddress, with that device current, and handed to
-// the unchanged fconv_run path as its workspace.
+// The workspace that fconv_run takes from the caller (the weight copy, the repacked X and
+// the split-K partial sums of the tensor-core route) comes here from one fixed, file-scope
+// device array. Host code never uses the array's name as an address (on the host it is
+// only a stand-in symbol): the device address is looked up once per device with
+// cudaGetSymbolAddress, with that device current, and handed to the unchanged fconv_run
+// path as its workspace. Plans that need no workspace never look it up.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -49,6 +50,7 @@ extern "C" fconv_status fconv_run_noalloc(const fconv_plan* plan, const void* x,
   fconv_status st = fconv_plan_workspace_size(plan, &need);
   if (st != FCONV_OK) return st;
   if (need > (size_t)FCONV_NOALLOC_SCRATCH_BYTES) return FCONV_E_WORKSPACE;
+  if (need == 0) return fconv_run(plan, x, w, b, z, y, nullptr, 0, stream);
   void* scratch = nullptr;
   st = scratch_for_current_device(&scratch);
   if (st != FCONV_OK) return st;

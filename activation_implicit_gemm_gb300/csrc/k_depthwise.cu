@@ -464,6 +464,7 @@ int launch_dw_t(const ConvGeom& g, const ConvArgs& a, cudaStream_t s) {
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem);                  \
     long long grid = (long long)sms * (per_sm > 0 ? per_sm : 1);                                \
     if (grid > planes) grid = planes;                                                           \
+    if (g.max_ctas > 0 && grid > g.max_ctas) grid = g.max_ctas;                                 \
     return launch_pdl(k, dim3((unsigned)grid), dim3(threads), smem, s, g, x, w, b, z, y, TR, TC, \
                       pitch, planes);                                                           \
   }

@@ -41,8 +41,9 @@
 // splits in a fixed order, then applies B, Z and the activation (deterministic).
 //
 // Every mbarrier wait is bounded in time (2 s); a wait that gives up sets a shared abort
-// flag and the device error word, and the CTA stops issuing work, drains its MMAs,
-// frees TMEM and exits.
+// flag and the device error word, and the CTA stops issuing work, waits (with a limit of
+// its own, ignoring the flag) for the MMAs and TMA loads it already issued, frees TMEM and
+// exits.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -150,6 +151,31 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
       }
     }
   }
+}
+
+// Wait for operations this CTA has already issued (MMAs behind a commit, TMA loads behind an
+// armed barrier). Issued operations always complete, so this wait ignores the abort flag and
+// only stops at its own time limit (then it records the timeout and returns).
+constexpr uint64_t kDrainLimitNs = 200000000ull;
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  if (ptx::mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (ptx::mbar_try_wait(bar, parity)) return;
+    if ((i & 63u) == 0 && ptx::globaltimer_ns() - t0 > kDrainLimitNs) {
+      atomicOr(&g_device_error, kErrWaitTimeout);
+      return;
+    }
+  }
+}
+
+// A TMA producer that stops early (abort) waits for the loads it issued: chunks [0, armed)
+// went to stage chunk % S with phase parity (chunk / S) & 1; a chunk whose phase already
+// completed returns at once.
+__device__ __forceinline__ void drain_armed(const uint64_t* full, uint32_t armed, int S) {
+  const uint32_t s = (uint32_t)S;
+  for (uint32_t j = armed > s ? armed - s : 0u; j < armed; ++j)
+    drain_wait(ptx::smem_addr(&full[j % s]), (j / s) & 1u);
 }
 
 // Bit t set when tap t of an axis lands inside X: 0 <= i0 + t * d < n, for k <= 32 taps.
@@ -592,6 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (stop) break;
       }
+      if (*abort_flag) drain_armed(ctl.full, it, S);
     }
   } else if (warp == kMmaWarp) {
     // ================================================================ MMA issue
@@ -628,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // every issued MMA must be complete before TMEM is freed
       ptx::mma_commit(ptx::smem_addr(&ctl.drain));
-      bounded_wait(ptx::smem_addr(&ctl.drain), 0, abort_flag);
+      drain_wait(ptx::smem_addr(&ctl.drain), 0);
     }
   } else {
     // ================================================================ epilogue (warps 0-15)
@@ -839,6 +866,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         }
         if (stop) break;
       }
+      if (*abort_flag) drain_armed(ctl.full, it, S);
     }
   } else if (warp == kTmaMmaWarp) {
     // ================================================================ MMA issue
@@ -874,7 +902,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         ptx::mma_commit(ptx::smem_addr(&ctl.acc_full[b]));
       }
       ptx::mma_commit(ptx::smem_addr(&ctl.drain));
-      bounded_wait(ptx::smem_addr(&ctl.drain), 0, abort_flag);
+      drain_wait(ptx::smem_addr(&ctl.drain), 0);
     }
   } else {
     // ================================================================ epilogue (warps 0-7)

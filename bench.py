@@ -136,7 +136,8 @@ class ClockSampler:
                 "samples": len(win)}
 
 
-def conv_tensors(case):
+def oracle_tensors(case):
+    """Inputs of one conv for the CPU legs (the oracle derives Y's shape for Z)."""
     import oracle
     ys = oracle.output_shape(case.x_shape, case.w_shape, **case.attrs())
     return workloads.make_inputs(case, ys), ys
@@ -175,10 +176,10 @@ def run_ours(args):
     if args.conv:
         cases = [workloads.case_by_name(n) for n in args.conv.split(",")]
     for case in cases:
-        t, ys = conv_tensors(case)
         dt = _lib.F16 if case.dtype == "f16" else _lib.F32
         plan = fc.FusedConvPlan(dt, case.x_shape, case.w_shape, has_bias=case.has_bias,
                                 has_z=case.has_z, device=local, **case.attrs())
+        t = workloads.make_inputs(case, plan.y_shape)
         d = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).to(dev))
              for k, v in t.items()}
         h = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).pin_memory())
@@ -424,7 +425,7 @@ def cpu_baseline():
     flops = 0.0
     secs = 0.0
     for case in workloads.ALL_CASES:
-        t, _ = conv_tensors(case)
+        t, _ = oracle_tensors(case)
         t0 = time.perf_counter()
         y, _ = oracle.fused_conv(t["x"], t["w"], t["b"], t["z"], **case.attrs())
         secs += time.perf_counter() - t0

@@ -139,6 +139,9 @@ typedef struct {
   int a_path;                   /* IGEMM_TC A operand: 0 = choose, 1 = in-kernel gather from
                                    X, 2 = TMA boxes of X repacked in 64-channel blocks (needs
                                    C/group % 64 == 0 and strides <= 8) */
+  int max_ctas;                 /* 0 = as many persistent CTAs as the work and the SMs allow;
+                                   else at most this many (the persistent kernels then walk
+                                   more work units per CTA) */
 } fconv_options;
 
 typedef struct fconv_plan fconv_plan;
@@ -205,8 +208,11 @@ fconv_status fconv_check_device(void* stream);
  *  - A plan needing more scratch than FCONV_NOALLOC_SCRATCH_BYTES is rejected with
  *    FCONV_E_WORKSPACE before anything is launched.
  *  - The device is the current CUDA device; x, w, b, z, y and `stream` must belong to it.
- *    The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *    The first call on a device whose plan needs a workspace looks up the array's device
+ *    address (cudaGetSymbolAddress) and keeps it; make that first call before any stream
+ *    capture. Plans that need no workspace (direct and depthwise routes) never touch the
+ *    array. The kept address does not survive cudaDeviceReset: do not use this entry
+ *    point again in a process after resetting the device.
  *  - Calls share the one array per device. It keeps the last call's contents; the
  *    kernels overwrite every scratch element they later read, so nothing is cleared.
  *    Calls whose kernels overlap on the GPU (other streams, other host threads) race on

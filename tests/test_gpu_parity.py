@@ -4,8 +4,12 @@ element, on identical seeded inputs.
 * small cases that span several tiles and ragged tails, for every route, tile width,
   split-K factor, rank, stride/dilation/padding mode, group and activation;
 * the benchmark convolutions at full size, in the launch configuration the benchmark
-  times, compared on the first and last image of the batch (every output of those
-  images);
+  times, every output of every image compared;
+* the persistent kernels with their grid capped at 1-3 CTAs, so that each CTA walks many
+  work units (every TMEM accumulator, every epilogue set, the operand ring's and the
+  accumulators' phase wraps, the depthwise kernel's double buffer);
+* exact results: integer-valued X, W, B, Z give exact sums, so the GPU output must equal
+  the oracle bit for bit on every route;
 * Y guard bands and NaN pre-fill catch out-of-bounds and missing writes.
 """
 import math
@@ -59,10 +63,11 @@ def gpu_run(plan: FusedConvPlan, xd, wd, bd, zd, dtype) -> np.ndarray:
 
 
 def compare(dtype, x, w, b, z, attrs, route="auto", split_k=0, tile_n=0, what="",
-            a_path="auto"):
+            a_path="auto", max_ctas=0):
     dt = _lib.F16 if dtype == "f16" else _lib.F32
     plan = FusedConvPlan(dt, x.shape, w.shape, has_bias=b is not None, has_z=z is not None,
-                         route=route, split_k=split_k, tile_n=tile_n, a_path=a_path, **attrs)
+                         route=route, split_k=split_k, tile_n=tile_n, a_path=a_path,
+                         max_ctas=max_ctas, **attrs)
     y = gpu_run(plan, to_dev(x), to_dev(w), to_dev(b), to_dev(z), dtype)
     ref, absacc = oracle.fused_conv(x, w, b, z, **attrs)
     pre = None
@@ -239,26 +244,95 @@ def test_direct_f32_random(sr):
         compare("f32", x, w, b, z, attrs, route="direct", what=f"direct f32 {sr}/{it}")
 
 
+# ----------------------------------------------------------------------------- persistent loops
+
+PERSISTENT_CASES = [
+    # (x_shape, w_shape, attrs, route, a_path, tile_n, split_k): enough work units that a
+    # capped grid walks every accumulator buffer and epilogue set several times
+    ((4, 16, 20, 20), (40, 16, 3, 3), dict(pads=[1, 1, 1, 1], activation="QuickGelu"),
+     "igemm_tc", "gather", 16, 1),
+    ((4, 16, 20, 20), (40, 16, 3, 3), dict(pads=[1, 1, 1, 1]), "igemm_tc", "gather", 64, 2),
+    ((3, 5, 23, 21), (130, 5, 3, 3), dict(pads=[1, 1, 1, 1], activation="HardSwish"),
+     "igemm_tc", "gather", 128, 1),
+    ((2, 8, 30, 31), (200, 8, 3, 3), dict(pads=[0, 1, 2, 1]), "igemm_tc", "gather", 256, 1),
+    ((6, 64, 12, 12), (48, 64, 3, 3), dict(pads=[1, 1, 1, 1], activation="Gelu"),
+     "igemm_tc", "tma", 16, 1),
+    ((6, 64, 12, 12), (80, 64, 3, 3), dict(pads=[1, 1, 1, 1]), "igemm_tc", "tma", 64, 3),
+    ((5, 128, 6, 6), (256, 128, 3, 3), dict(pads=[1, 1, 1, 1]), "igemm_tc", "tma", 256, 1),
+    ((6, 16, 24, 24), (16, 1, 3, 3), dict(group=16, pads=[1, 1, 1, 1], activation="Relu"),
+     "depthwise", "auto", 0, 0),
+    ((3, 8, 40, 36), (8, 1, 7, 7), dict(group=8, pads=[3, 3, 3, 3]), "depthwise", "auto", 0, 0),
+]
+
+
+@pytest.mark.parametrize("max_ctas", [1, 2, 3])
+@pytest.mark.parametrize("idx", range(len(PERSISTENT_CASES)))
+def test_persistent_loop(idx, max_ctas):
+    xs, ws, attrs, route, a_path, tile_n, split_k = PERSISTENT_CASES[idx]
+    x, w, b, z = inputs(1200 + 10 * idx + max_ctas, "f16", xs, ws, True, True, attrs)
+    compare("f16", x, w, b, z, attrs, route=route, a_path=a_path, tile_n=tile_n,
+            split_k=split_k, max_ctas=max_ctas, what=f"persistent {idx} ctas={max_ctas}")
+
+
+# ----------------------------------------------------------------------------- exact results
+
+EXACT_CASES = [
+    # (dtype, x_shape, w_shape, attrs, route, options, w range): integer X in [-2, 2],
+    # B and Z in [-2, 2]; every |sum| stays below 2048, so f16 holds it exactly
+    ("f16", (2, 12, 10, 9), (20, 12, 3, 3), dict(pads=[1, 1, 1, 1]), "igemm_tc",
+     dict(a_path="gather"), 2),
+    ("f16", (2, 12, 10, 9), (20, 12, 3, 3), dict(pads=[1, 1, 1, 1]), "igemm_tc",
+     dict(a_path="gather", split_k=3), 2),
+    ("f16", (3, 3, 17, 15), (16, 3, 5, 5), dict(strides=[2, 2], pads=[2, 2, 2, 2]), "igemm_tc",
+     dict(a_path="gather"), 2),
+    ("f16", (2, 64, 6, 7), (32, 64, 3, 3), dict(pads=[1, 1, 1, 1]), "igemm_tc",
+     dict(a_path="tma"), 1),
+    ("f16", (2, 64, 6, 7), (32, 64, 3, 3), dict(pads=[1, 1, 1, 1]), "igemm_tc",
+     dict(a_path="tma", split_k=2), 1),
+    ("f16", (2, 8, 14, 14), (8, 1, 7, 7), dict(group=8, pads=[3, 3, 3, 3]), "depthwise", {}, 2),
+    ("f16", (2, 6, 9, 8), (9, 2, 3, 3), dict(group=3, pads=[1, 1, 1, 1]), "direct", {}, 2),
+    ("f32", (2, 6, 9, 8), (9, 2, 3, 3), dict(group=3, pads=[1, 1, 1, 1]), "direct", {}, 2),
+    ("f32", (2, 3, 5, 9, 8), (4, 3, 3, 3, 3), dict(strides=[1, 2, 1], auto_pad="SAME_UPPER"),
+     "direct", {}, 2),
+    ("f32", (2, 8, 14, 14), (8, 1, 3, 3), dict(group=8, pads=[1, 1, 1, 1]), "depthwise", {}, 2),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(EXACT_CASES)))
+def test_exact_integer_results(idx):
+    """Integer-valued inputs: the convolution's sums are exact in f32 accumulation and in
+    the oracle's fp64, so every output must be identical (no activation applied)."""
+    dtype, xs, wsh, attrs, route, opts, wr = EXACT_CASES[idx]
+    ys = oracle.output_shape(xs, wsh, **attrs)
+    x = workloads.draw_int(1400 + 4 * idx, xs, -2, 2, dtype)
+    w = workloads.draw_int(1401 + 4 * idx, wsh, -wr, wr, dtype)
+    b = workloads.draw_int(1402 + 4 * idx, (wsh[0],), -2, 2, dtype)
+    z = workloads.draw_int(1403 + 4 * idx, ys, -2, 2, dtype)
+    dt = _lib.F16 if dtype == "f16" else _lib.F32
+    plan = FusedConvPlan(dt, xs, wsh, has_bias=True, has_z=True, route=route, **opts, **attrs)
+    y = gpu_run(plan, to_dev(x), to_dev(w), to_dev(b), to_dev(z), dtype)
+    ref, absacc = oracle.fused_conv(x, w, b, z, **attrs)
+    assert float(np.abs(ref).max()) < 2048.0
+    assert np.array_equal(ref, np.round(ref)), "the oracle's sums of integers are integers"
+    bad = y != ref
+    assert not bad.any(), (f"exact case {idx} ({plan.route}): {int(bad.sum())} of {bad.size} "
+                           f"outputs differ, first at {tuple(np.argwhere(bad)[0])}")
+
+
 # ----------------------------------------------------------------------------- full-size configs
 
 @pytest.mark.parametrize("name", [c.name for c in workloads.ALL_CASES])
 def test_config_full_size(name):
-    """Auto-planned run at full size; every output of the first and last image checked."""
+    """Auto-planned run at full size, in the launch configuration the benchmark times;
+    every output of every image compared with the oracle."""
     c = workloads.case_by_name(name)
     attrs = c.attrs()
-    ys = oracle.output_shape(c.x_shape, c.w_shape, **attrs)
-    t = workloads.make_inputs(c, ys)
     dt = _lib.F16 if c.dtype == "f16" else _lib.F32
     plan = FusedConvPlan(dt, c.x_shape, c.w_shape, has_bias=c.has_bias, has_z=c.has_z, **attrs)
+    t = workloads.make_inputs(c, plan.y_shape)
     y = gpu_run(plan, to_dev(t["x"]), to_dev(t["w"]), to_dev(t["b"]), to_dev(t["z"]), c.dtype)
-    N = c.x_shape[0]
-    sample = sorted({0, N - 1})
-    xs = t["x"][sample]
-    zs = None if t["z"] is None else t["z"][sample]
-    ref, absacc = oracle.fused_conv(xs, t["w"], t["b"], zs, **attrs)
-    pre = None
+    ref, absacc = oracle.fused_conv(t["x"], t["w"], t["b"], t["z"], **attrs)
     kg = int(np.prod(c.w_shape[1:]))
     alpha = (attrs.get("activation_params") or [1.0])[0]
-    check(y[sample], ref, absacc, c.dtype, kg, activation=attrs.get("activation"), alpha=alpha,
-          pre_act=pre, what=f"{name} route={plan.route} split={plan.split_k}")
-    assert np.isfinite(y).all()
+    check(y, ref, absacc, c.dtype, kg, activation=attrs.get("activation"), alpha=alpha,
+          what=f"{name} route={plan.route} split={plan.split_k}")

@@ -1,11 +1,14 @@
 """fconv_run_noalloc: the entry point for callers that cannot allocate device memory
 (code inside allocator hooks or captures that must not allocate, host callbacks,
-plugins whose host application owns every device allocation). Its split-K scratch is a
-fixed array inside the library instead of a caller-supplied workspace.
+plugins whose host application owns every device allocation). The workspace a
+tensor-core plan needs (the weight copy in GEMM order, X repacked for the A operand and
+any split-K partial sums) comes from a fixed array inside the library instead of a
+caller-supplied buffer.
 
-Checked through the C ABI against fconv_run (the caller-workspace entry point) on
-the same plan and inputs, on two calls in a row, with another plan run in between so
-the shared scratch holds a different call's leftovers. This file is collected last.
+Each plan runs through the C ABI on two calls in a row, with another plan run in between
+so the shared array holds a different call's leftovers. Every output is compared with
+fconv_run (the caller-workspace entry point) on the same plan and inputs, and with the
+oracle, within the parity tolerance. This file is collected last.
 """
 import ctypes
 import math
@@ -17,7 +20,7 @@ import torch
 import oracle
 import workloads
 from activation_implicit_gemm_gb300 import FusedConvPlan, _build, _lib
-from parity import tolerance
+from parity import check, tolerance
 
 pytestmark = pytest.mark.gpu
 
@@ -42,22 +45,34 @@ def seeded(seed, x_shape, w_shape, attrs):
     return x, w, b, z
 
 
-def test_noalloc_matches_fconv_run_on_two_calls():
+PLANS = [
+    # (x_shape, w_shape, attrs, options): gathered A with split-K partials
+    ((2, 32, 19, 21), (48, 32, 3, 3), dict(pads=[1, 1, 1, 1], activation="Gelu"),
+     dict(split_k=3)),
+    # C/group a multiple of 64: TMA boxes over X repacked in the array, split K
+    ((3, 64, 8, 8), (40, 64, 3, 3), dict(pads=[1, 1, 1, 1], activation="QuickGelu"),
+     dict(split_k=2, a_path="tma")),
+    # the same without split-K
+    ((2, 128, 9, 7), (72, 128, 3, 3), dict(pads=[1, 0, 1, 1]), dict(a_path="tma")),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(PLANS)))
+def test_noalloc_matches_fconv_run_and_oracle_on_two_calls(idx):
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
     _build.build()
     run_noalloc = noalloc_fn()
     stream = torch.cuda.current_stream().cuda_stream
 
-    attrs = dict(pads=[1, 1, 1, 1], activation="Gelu")
-    xs, wsh = (2, 32, 19, 21), (48, 32, 3, 3)
+    xs, wsh, attrs, opts = PLANS[idx]
     plan = FusedConvPlan(_lib.F16, xs, wsh, has_bias=True, has_z=True, route="igemm_tc",
-                         split_k=3, **attrs)
-    assert plan.split_k == 3 and 0 < plan.workspace_bytes <= SCRATCH_BYTES
-    x, w, b, z = seeded(31, xs, wsh, attrs)
+                         **opts, **attrs)
+    assert 0 < plan.workspace_bytes <= SCRATCH_BYTES
+    x, w, b, z = seeded(31 + 10 * idx, xs, wsh, attrs)
     xd, wd, bd, zd = (torch.from_numpy(a).cuda() for a in (x, w, b, z))
 
-    # the other plan, run through the no-allocation entry point between the two calls
+    # another plan, run through the no-allocation entry point between the two calls
     attrs2 = dict(strides=[2, 2], pads=[1, 1, 1, 1], activation="Relu")
     xs2, wsh2 = (3, 16, 30, 17), (64, 16, 3, 3)
     plan2 = FusedConvPlan(_lib.F16, xs2, wsh2, has_bias=True, has_z=True, route="igemm_tc",
@@ -65,11 +80,12 @@ def test_noalloc_matches_fconv_run_on_two_calls():
     x2, w2, b2, z2 = seeded(41, xs2, wsh2, attrs2)
     d2 = [torch.from_numpy(a).cuda() for a in (x2, w2, b2, z2)]
 
-    y_ref = plan.run(xd, wd, bd, zd)  # existing entry point, torch-allocated workspace
+    y_run = plan.run(xd, wd, bd, zd)  # the caller-workspace entry point
     torch.cuda.synchronize()
-    _, absacc = oracle.fused_conv(x, w, b, z, **attrs)
-    ref = y_ref.double().cpu().numpy()
-    tol = tolerance(ref, absacc, "f16", int(np.prod(wsh[1:])))
+    ref_run = y_run.double().cpu().numpy()
+    ref, absacc = oracle.fused_conv(x, w, b, z, **attrs)
+    kg = int(np.prod(wsh[1:]))
+    tol = tolerance(ref, absacc, "f16", kg)
 
     for call in range(2):
         y = torch.full(plan.y_shape, float("nan"), dtype=torch.float16, device="cuda")
@@ -78,8 +94,10 @@ def test_noalloc_matches_fconv_run_on_two_calls():
         assert _lib.STATUS[st] == "OK", f"call {call}: {_lib.STATUS[st]}"
         torch.cuda.synchronize()
         got = y.double().cpu().numpy()
-        err = np.abs(got - ref)
-        assert np.all(err <= tol), f"call {call}: max err {err.max():.3e}"
+        err = np.abs(got - ref_run)
+        assert np.all(err <= tol), f"call {call} vs fconv_run: max err {err.max():.3e}"
+        check(got, ref, absacc, "f16", kg, activation=attrs.get("activation"),
+              what=f"noalloc plan {idx} call {call} vs oracle")
         y2 = torch.empty(plan2.y_shape, dtype=torch.float16, device="cuda")
         st = run_noalloc(plan2._ptr, *(t.data_ptr() for t in d2), y2.data_ptr(), stream)
         assert _lib.STATUS[st] == "OK"
@@ -106,3 +124,25 @@ def test_noalloc_rejects_plans_beyond_the_scratch_size():
     assert _lib.STATUS[st] == "E_WORKSPACE"
     torch.cuda.synchronize()
     assert bool((y == 3.0).all())
+
+
+def test_noalloc_runs_workspace_free_routes():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    _build.build()
+    run_noalloc = noalloc_fn()
+    attrs = dict(group=8, pads=[1, 1, 1, 1], activation="Clip", activation_params=[-1.0, 1.0])
+    xs, wsh = (2, 8, 12, 12), (8, 1, 3, 3)
+    plan = FusedConvPlan(_lib.F16, xs, wsh, has_bias=True, has_z=True, route="depthwise",
+                         **attrs)
+    assert plan.workspace_bytes == 0
+    x, w, b, z = seeded(61, xs, wsh, attrs)
+    d = [torch.from_numpy(a).cuda() for a in (x, w, b, z)]
+    y = torch.empty(plan.y_shape, dtype=torch.float16, device="cuda")
+    st = run_noalloc(plan._ptr, *(t.data_ptr() for t in d), y.data_ptr(),
+                     torch.cuda.current_stream().cuda_stream)
+    assert _lib.STATUS[st] == "OK"
+    torch.cuda.synchronize()
+    ref, absacc = oracle.fused_conv(x, w, b, z, **attrs)
+    check(y.double().cpu().numpy(), ref, absacc, "f16", 9, activation="Clip",
+          what="noalloc depthwise")

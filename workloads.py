@@ -63,6 +63,15 @@ def draw(seed: int, shape: Sequence[int], dist: str, scale: float, dtype: str) -
     return v.astype(np_dt).reshape(shape)
 
 
+def draw_int(seed: int, shape: Sequence[int], lo: int, hi: int, dtype: str) -> np.ndarray:
+    """A seeded tensor of integers uniform in [lo, hi], stored as `dtype` ('f16' or 'f32')."""
+    n = int(np.prod(shape)) if len(shape) else 1
+    span = hi - lo + 1
+    v = np.minimum(np.floor(uniform01(seed, n) * span), span - 1) + lo
+    np_dt = np.float16 if dtype == "f16" else np.float32
+    return v.astype(np_dt).reshape(shape)
+
+
 @dataclasses.dataclass(frozen=True)
 class ConvCase:
     """One FusedConv call: shapes, attributes and the value distributions of its inputs."""
