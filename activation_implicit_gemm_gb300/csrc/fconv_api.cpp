@@ -167,22 +167,17 @@ fconv_status resolve(const fconv_desc* d, fconv_plan* p) {
   return FCONV_OK;
 }
 
-int pick_tile_n(int Mg) {
-  static const int tiles[] = {16, 32, 64, 128, 256};
-  for (int t : tiles)
-    if (Mg <= t) return t;
-  return 256;
-}
+// Largest pixel tile (MMA N) of the tensor-core kernels; channel tiles are always 128.
+constexpr int kDefaultPixelTile = 256;
 
 void plan_igemm(fconv_plan* p, const fconv_options* o) {
   const ConvGeom& g = p->g;
   IgemmConfig& c = p->igemm;
-  c.tile_n = (o && o->tile_n) ? o->tile_n : pick_tile_n(g.Mg);
-  c.stages = igemm_tc_stages(c.tile_n);
-  c.a_path = o ? o->a_path : 0;
-  const long long rows = igemm_tc_mtiles(g, c.a_path);
-  const long long tiles = rows * ((g.Mg + c.tile_n - 1) / c.tile_n) * g.G;
-  const int chunks = igemm_tc_chunks(g, c.a_path);
+  c.tile_n = (o && o->tile_n) ? o->tile_n : kDefaultPixelTile;
+  c.a_path = igemm_tc_resolve_path(g, c.tile_n, o ? o->a_path : 0);
+  const long long rows = igemm_tc_mtiles(g, c.a_path, c.tile_n);
+  const long long tiles = rows * ((g.Mg + 127) / 128) * g.G;
+  const int chunks = igemm_tc_chunks(g, c.a_path, c.tile_n);
   int split = 1;
   if (o && o->split_k > 0) {
     split = o->split_k;
@@ -227,24 +222,24 @@ fconv_status create(const fconv_desc* d, int device, const fconv_options* o, fco
   p->g.max_ctas = o ? o->max_ctas : 0;
   const fconv_route want = o ? o->route : FCONV_ROUTE_AUTO;
   fconv_route route = want;
+  const int tile_n = (o && o->tile_n) ? o->tile_n : kDefaultPixelTile;
   if (want == FCONV_ROUTE_AUTO) {
     if (depthwise_supported(p->g)) route = FCONV_ROUTE_DEPTHWISE;
-    else if (igemm_tc_supported(p->g)) route = FCONV_ROUTE_IGEMM_TC;
+    else if (igemm_tc_supported(p->g, tile_n)) route = FCONV_ROUTE_IGEMM_TC;
     else route = FCONV_ROUTE_DIRECT;
   } else if (want == FCONV_ROUTE_DEPTHWISE && !depthwise_supported(p->g)) {
     st = FCONV_E_UNSUPPORTED;
-  } else if (want == FCONV_ROUTE_IGEMM_TC && !igemm_tc_supported(p->g)) {
+  } else if (want == FCONV_ROUTE_IGEMM_TC && !igemm_tc_supported(p->g, tile_n)) {
     st = FCONV_E_UNSUPPORTED;
   } else if (want != FCONV_ROUTE_DIRECT && want != FCONV_ROUTE_DEPTHWISE &&
              want != FCONV_ROUTE_IGEMM_TC) {
     st = FCONV_E_UNSUPPORTED;
   }
-  if (st == FCONV_OK && route == FCONV_ROUTE_IGEMM_TC && o &&
-      (o->a_path < 0 || o->a_path > 2 || (o->a_path == 2 && !igemm_tc_tma_capable(p->g)) ||
-       (o->a_path == 1 && !igemm_tc_gather_capable(p->g))))
-    st = FCONV_E_UNSUPPORTED;
   if (st == FCONV_OK && route == FCONV_ROUTE_IGEMM_TC && o && o->tile_n &&
-      (o->tile_n < 16 || o->tile_n > 256 || (o->tile_n & (o->tile_n - 1)) != 0))
+      o->tile_n != 64 && o->tile_n != 128 && o->tile_n != 256)
+    st = FCONV_E_UNSUPPORTED;
+  if (st == FCONV_OK && route == FCONV_ROUTE_IGEMM_TC && o &&
+      (o->a_path < 0 || o->a_path > 2 || igemm_tc_resolve_path(p->g, tile_n, o->a_path) == 0))
     st = FCONV_E_UNSUPPORTED;
   if (st != FCONV_OK) {
     delete p;

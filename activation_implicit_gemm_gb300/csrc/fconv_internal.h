@@ -1,6 +1,7 @@
 // Internal interface between the planner (fconv_api.cpp) and the CUDA launchers.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -44,27 +45,47 @@ struct ConvArgs {
 
 // Tensor-core implicit GEMM configuration.
 struct IgemmConfig {
-  int tile_n;      // MMA N (channels per tile): 16..256, multiple of 16
+  int tile_n;      // largest pixel tile (MMA N): 64, 128 or 256; channel tiles are 128
   int split_k;     // number of K splits (>= 1)
-  int stages;      // shared-memory pipeline depth (even)
   long long grid;  // persistent CTAs (one per SM at most)
-  int a_path;      // 0 auto, 1 in-kernel gather of A, 2 TMA boxes of repacked X
+  int a_path;      // 1: im2col rows built in-kernel from the NC(D)HW input patch
+                   //    (k_igemm_patch.cu); 2: TMA boxes of X repacked in 64-channel blocks
+                   //    (k_igemm_tc.cu)
 };
 
 // Launchers: return cudaError_t as int (0 = success).
 int launch_direct(const ConvGeom& g, const ConvArgs& a, void* stream);
 int launch_depthwise(const ConvGeom& g, const ConvArgs& a, void* stream);
-int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, void* stream);
-bool igemm_tc_supported(const ConvGeom& g);
 bool depthwise_supported(const ConvGeom& g);
-int igemm_tc_stages(int tile_n);
-size_t igemm_tc_smem_bytes(int tile_n, int stages);
+
+// tcgen05 implicit GEMM: dispatch between the two A paths (k_igemm_tc.cu).
+int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, void* stream);
+bool igemm_tc_supported(const ConvGeom& g, int max_px);    // some im2col path runs the request
+bool igemm_tc_tma_capable(const ConvGeom& g);             // the TMA-fed path runs it
+// The im2col path for a request (0 auto, 1 patch, 2 TMA-fed): 1 or 2, or 0 when none can.
+int igemm_tc_resolve_path(const ConvGeom& g, int max_px, int requested);
 size_t igemm_tc_workspace_bytes(const ConvGeom& g, const IgemmConfig& c);
-long long igemm_tc_mtiles(const ConvGeom& g, int a_path);  // pixel tiles of the A operand
-int igemm_tc_chunks(const ConvGeom& g, int a_path);        // 64-wide K chunks of the GEMM
-bool igemm_tc_tma_capable(const ConvGeom& g);             // TMA-fed A path possible
-bool igemm_tc_gather_capable(const ConvGeom& g);          // gathered A path possible
+long long igemm_tc_mtiles(const ConvGeom& g, int a_path, int max_px);  // pixel tiles
+int igemm_tc_chunks(const ConvGeom& g, int a_path, int max_px);        // 64-wide K chunks
 int igemm_tc_launches(const ConvGeom& g, const IgemmConfig& c);  // kernels per fconv_run
+int launch_splitk_reduce(const ConvGeom& g, int splits, const float* part, const void* b,
+                         const void* z, void* y, void* stream);
+
+// The patch-fed kernel (k_igemm_patch.cu).
+bool igemm_patch_capable(const ConvGeom& g, int tile_n);
+long long igemm_patch_mtiles(const ConvGeom& g, int tile_n);
+int igemm_patch_chunks(const ConvGeom& g, int tile_n);
+size_t igemm_patch_workspace_bytes(const ConvGeom& g, const IgemmConfig& c);
+int igemm_patch_launches(const ConvGeom& g, const IgemmConfig& c);
+int launch_igemm_patch(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, void* stream);
+int read_and_clear_patch_error(void* stream, unsigned* value);
+
+// cuTensorMapEncodeTiled from the driver (null when unavailable).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
 
 // Launch with programmatic stream serialization: the kernel may begin (and run up to its
 // pdl_wait()) while the previous kernel in the stream finishes.

@@ -150,9 +150,9 @@ def bound_of(flops, bytes_, peaks):
 
 def main_kernel_name(case, route):
     """The kernel that does the conv's arithmetic (the TMA-fed implicit GEMM takes
-    C/group a multiple of 64; other tensor-core convs gather their A operand)."""
+    C/group a multiple of 64; other tensor-core convs build A from the input patch)."""
     if route == "igemm_tc":
-        return "igemm_tma_kernel" if case.w_shape[1] % 64 == 0 else "igemm_tc_kernel"
+        return "igemm_tma_kernel" if case.w_shape[1] % 64 == 0 else "igemm_patch_kernel"
     return {"depthwise": "dw_kernel_persistent", "direct": "direct_conv_kernel"}[route]
 
 

@@ -135,7 +135,9 @@ typedef struct {
 typedef struct {
   fconv_route route;            /* FCONV_ROUTE_AUTO = choose */
   int split_k;                  /* 0 = choose; >= 1 forces that many K splits (IGEMM_TC) */
-  int tile_n;                   /* 0 = choose; else the tensor-core N tile (16..256, %16) */
+  int tile_n;                   /* 0 = choose; else the largest pixel tile (MMA N) of the
+                                   tensor-core kernels: 64, 128 or 256 (their channel tiles
+                                   are 128) */
   int a_path;                   /* IGEMM_TC A operand: 0 = choose, 1 = in-kernel gather from
                                    X, 2 = TMA boxes of X repacked in 64-channel blocks (needs
                                    C/group % 64 == 0 and strides <= 8) */

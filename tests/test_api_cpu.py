@@ -168,9 +168,9 @@ def test_split_k_planned_for_small_grids(lib):
 
 
 def test_forced_routes(lib):
-    p = FusedConvPlan(_lib.F16, (1, 8, 9, 9), (16, 8, 3, 3), route="igemm_tc", tile_n=32,
+    p = FusedConvPlan(_lib.F16, (1, 8, 9, 9), (16, 8, 3, 3), route="igemm_tc", tile_n=128,
                       split_k=2)
-    assert (p.route, p.tile_n, p.split_k) == ("igemm_tc", 32, 2)
+    assert (p.route, p.tile_n, p.split_k) == ("igemm_tc", 128, 2)
     with pytest.raises(FconvError) as e:
         FusedConvPlan(_lib.F32, (1, 8, 9, 9), (16, 8, 3, 3), route="igemm_tc")
     assert e.value.code == "E_UNSUPPORTED"
@@ -179,6 +179,9 @@ def test_forced_routes(lib):
     assert e.value.code == "E_UNSUPPORTED"
     with pytest.raises(FconvError) as e:
         FusedConvPlan(_lib.F16, (1, 8, 9, 9), (16, 8, 3, 3), route="igemm_tc", tile_n=48)
+    assert e.value.code == "E_UNSUPPORTED"
+    with pytest.raises(FconvError) as e:  # pixel tiles are 64, 128 or 256
+        FusedConvPlan(_lib.F16, (1, 8, 9, 9), (16, 8, 3, 3), route="igemm_tc", tile_n=32)
     assert e.value.code == "E_UNSUPPORTED"
 
 
@@ -237,17 +240,34 @@ def test_invariant_divisor_arithmetic(lib):
 
 
 def test_launch_counts_and_workspace_regions(lib):
-    # tensor-core route: a prologue launch (weight copy + X repack) and the implicit GEMM,
-    # plus the reduction when K is split; the workspace holds exactly those buffers
+    # patch-fed tensor-core kernel: one launch, no workspace (X is read as it is, the
+    # weights are resident or read as they are)
     ca = workloads.case_by_name("cnn_a_3to64_32x32")
     p = FusedConvPlan(_lib.F16, ca.x_shape, ca.w_shape, **ca.attrs())
-    assert p.route == "igemm_tc" and p.split_k == 1 and p.launches == 2
-    # gathered A: X channels-last with 3 channels padded to 4; weights in (tap, channel)
-    # order, 9 taps x 4 channels padded to a multiple of 8 columns
-    wcopy = (2 * 64 * 40 + 1023) // 1024 * 1024
-    xcopy = (2 * 512 * 32 * 32 * 4 + 1023) // 1024 * 1024
-    assert p.workspace_bytes == wcopy + xcopy
-    ps = FusedConvPlan(_lib.F16, (1, 256, 8, 8), (128, 256, 3, 3), pads=[1, 1, 1, 1])
+    assert p.route == "igemm_tc" and p.split_k == 1 and p.launches == 1
+    assert p.workspace_bytes == 0
+    # a split plan adds the f32 partial sums and the reduction launch
+    pk = FusedConvPlan(_lib.F16, (2, 16, 9, 9), (24, 16, 3, 3), pads=[1, 1, 1, 1],
+                       route="igemm_tc", a_path="gather", split_k=3)
+    assert pk.split_k == 3 and pk.launches == 2
+    assert pk.workspace_bytes == 3 * 4 * 2 * 24 * 81
+    # weights too large to keep resident with a row length that is not a multiple of 8
+    # elements: a padded copy for the TMA boxes, written by its own launch
+    pw = FusedConvPlan(_lib.F16, (1, 5, 9, 9), (1024, 5, 3, 3), pads=[1, 1, 1, 1],
+                       route="igemm_tc", a_path="gather")
+    assert pw.launches == 2 and pw.workspace_bytes == (1024 * 48 * 2 + 1023) // 1024 * 1024
+    # TMA-fed kernel (C/group a multiple of 64): a prologue launch (weight copy in the
+    # 64-channel block order + X repacked into 64-channel blocks) and the implicit GEMM,
+    # plus the reduction when K is split; the workspace holds exactly those buffers
+    cb = workloads.case_by_name("cnn_b_64to128_16x16_z")
+    pt = FusedConvPlan(_lib.F16, cb.x_shape, cb.w_shape, has_z=True, route="igemm_tc",
+                       a_path="tma", **cb.attrs())
+    assert pt.launches == 2
+    wcopy = (2 * 128 * 576 + 1023) // 1024 * 1024
+    xcopy = (2 * 512 * 64 * 16 * 16 + 1023) // 1024 * 1024
+    assert pt.workspace_bytes == wcopy + xcopy
+    ps = FusedConvPlan(_lib.F16, (1, 256, 8, 8), (128, 256, 3, 3), pads=[1, 1, 1, 1],
+                       a_path="tma")
     assert ps.split_k > 1 and ps.launches == 3
     # one kernel and no workspace on the depthwise and direct routes
     cd = workloads.case_by_name("stem_dw_128_k7")

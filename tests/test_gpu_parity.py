@@ -93,22 +93,22 @@ def inputs(seed, dtype, x_shape, w_shape, bias, zres, attrs, wscale=None):
 
 # ----------------------------------------------------------------------------- tcgen05 path
 
-@pytest.mark.parametrize("tile_n", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("tile_n", [64, 128, 256])
 @pytest.mark.parametrize("split_k", [1, 2, 3])
 def test_tc_tiles_and_splits(tile_n, split_k):
-    # 2*11*13 = 286 pixels: 3 row tiles with a ragged tail; Mg = 40; Kg = 216: 4 chunks,
-    # the last one partial
+    # 2*11*13 = 286 pixels: several pixel tiles with a ragged tail (tile_n caps the pixel
+    # tile); Mg = 40 of a 128-channel tile; Kg = 216: 4 chunks, the last one partial
     attrs = dict(pads=[1, 1, 1, 1], activation="LeakyRelu", activation_params=[0.1])
     x, w, b, z = inputs(11, "f16", (2, 24, 11, 13), (40, 24, 3, 3), True, True, attrs)
     compare("f16", x, w, b, z, attrs, route="igemm_tc", tile_n=tile_n, split_k=split_k,
             what="tiles")
 
 
-@pytest.mark.parametrize("tile_n", [16, 64, 256])
+@pytest.mark.parametrize("tile_n", [64, 128, 256])
 @pytest.mark.parametrize("split_k", [1, 2])
 def test_tc_vector_epilogue_ragged(tile_n, split_k):
-    # P = 64 (a multiple of 8: 16-byte Y/Z path); 3*64 = 192 pixels: the second row tile
-    # is half empty; Mg = 40: the last 16-channel group has 8 valid channels
+    # P = 64 (a multiple of 8: 16-byte Y/Z path); 3*64 = 192 pixels: whole-image boxes with
+    # a partly filled last one; Mg = 40 of a 128-channel tile
     attrs = dict(pads=[1, 1, 1, 1], activation="QuickGelu")
     x, w, b, z = inputs(13, "f16", (3, 16, 8, 8), (40, 16, 3, 3), True, True, attrs)
     compare("f16", x, w, b, z, attrs, route="igemm_tc", tile_n=tile_n, split_k=split_k,
@@ -122,13 +122,14 @@ TMA_CASES = [
     ((2, 64, 13, 11), (72, 64, 3, 3), dict(pads=[1, 0, 2, 1]), True, True, 0, 0),      # ragged box
     ((2, 128, 16, 16), (48, 128, 3, 3), dict(pads=[1, 1, 1, 1], activation="Gelu"), False, True, 64, 2),
     ((2, 64, 20, 20), (64, 64, 2, 2), dict(strides=[2, 2]), True, False, 0, 0),        # stride 2
-    ((1, 64, 17, 19), (32, 64, 3, 3), dict(dilations=[2, 3], pads=[2, 3, 2, 3]), True, True, 32, 1),
+    ((1, 64, 17, 19), (32, 64, 3, 3), dict(dilations=[2, 3], pads=[2, 3, 2, 3]), True, True, 128, 1),
     ((2, 64, 300), (64, 64, 5), dict(dilations=[2], auto_pad="SAME_UPPER"), True, True, 0, 0),
     ((1, 64, 6, 9, 10), (16, 64, 3, 3, 3), dict(strides=[2, 2, 2], auto_pad="SAME_LOWER"), True, True, 0, 0),
     ((2, 128, 7, 9), (96, 64, 3, 3), dict(group=2, pads=[1, 1, 1, 1]), True, True, 0, 0),  # grouped
     ((9, 256, 4, 4), (320, 256, 3, 3), dict(pads=[1, 1, 1, 1], activation="HardSwish"), False, True, 256, 0),
     ((2, 64, 9, 9), (24, 64, 1, 1), dict(), True, False, 0, 0),                        # 1x1
-    ((2, 64, 12, 12), (16, 64, 3, 3), dict(strides=[3, 3], pads=[1, 1, 1, 1]), True, True, 16, 3),
+    ((2, 64, 12, 12), (16, 64, 3, 3), dict(strides=[3, 3], pads=[1, 1, 1, 1]), True, True, 64, 3),
+    ((2, 384, 6, 6), (300, 384, 3, 3), dict(pads=[1, 1, 1, 1], activation="Relu"), True, True, 0, 0),  # 3 channel tiles
 ]
 
 
@@ -250,14 +251,14 @@ PERSISTENT_CASES = [
     # (x_shape, w_shape, attrs, route, a_path, tile_n, split_k): enough work units that a
     # capped grid walks every accumulator buffer and epilogue set several times
     ((4, 16, 20, 20), (40, 16, 3, 3), dict(pads=[1, 1, 1, 1], activation="QuickGelu"),
-     "igemm_tc", "gather", 16, 1),
-    ((4, 16, 20, 20), (40, 16, 3, 3), dict(pads=[1, 1, 1, 1]), "igemm_tc", "gather", 64, 2),
+     "igemm_tc", "gather", 64, 1),
+    ((4, 16, 24, 24), (40, 16, 3, 3), dict(pads=[1, 1, 1, 1]), "igemm_tc", "gather", 64, 2),
     ((3, 5, 23, 21), (130, 5, 3, 3), dict(pads=[1, 1, 1, 1], activation="HardSwish"),
      "igemm_tc", "gather", 128, 1),
-    ((2, 8, 30, 31), (200, 8, 3, 3), dict(pads=[0, 1, 2, 1]), "igemm_tc", "gather", 256, 1),
+    ((2, 8, 30, 32), (200, 8, 3, 3), dict(pads=[0, 1, 2, 1]), "igemm_tc", "gather", 256, 1),
     ((6, 64, 12, 12), (48, 64, 3, 3), dict(pads=[1, 1, 1, 1], activation="Gelu"),
-     "igemm_tc", "tma", 16, 1),
-    ((6, 64, 12, 12), (80, 64, 3, 3), dict(pads=[1, 1, 1, 1]), "igemm_tc", "tma", 64, 3),
+     "igemm_tc", "tma", 64, 1),
+    ((6, 64, 12, 12), (80, 64, 3, 3), dict(pads=[1, 1, 1, 1]), "igemm_tc", "tma", 128, 3),
     ((5, 128, 6, 6), (256, 128, 3, 3), dict(pads=[1, 1, 1, 1]), "igemm_tc", "tma", 256, 1),
     ((6, 16, 24, 24), (16, 1, 3, 3), dict(group=16, pads=[1, 1, 1, 1], activation="Relu"),
      "depthwise", "auto", 0, 0),
