@@ -321,37 +321,41 @@ __global__ void __launch_bounds__(kPThreads, 1)
           }
           const int kin = (i0 + k) * kBK;
           const int len = min(kBK, kb - kin);
-#pragma unroll 1
-          for (int h = 0; h < nrow; ++h) {
-            const uint32_t arow = base + st.idx * a.stage_bytes + wst + roff[h];
-            const uint32_t swz = (roff[h] >> 7) & 7u;
-            const int nunits = ((len + 15) >> 4) * 2;  // 16-byte units the MMAs read
-            if (row_zero[h]) {
-              for (int uu = 0; uu < nunits; ++uu)
-                ptx::st_shared_v4(arow + (((uint32_t)uu ^ swz) << 4), 0u, 0u, 0u, 0u);
-              continue;
-            }
-            if (!row_ok[h]) continue;
-            const uint32_t src = pslot + 2u * (uint32_t)(rbase[h] + ao);
-            const int* tk = tab + kin;
-#pragma unroll 1
-            for (int uu = 0; uu < nunits; ++uu) {
-              const int k0 = 8 * uu;
-              const int4 t0 = *reinterpret_cast<const int4*>(tk + k0);
-              const int4 t1 = *reinterpret_cast<const int4*>(tk + k0 + 4);
-              uint32_t e[8];
-              if (k0 + 8 <= len) {
-                e[0] = ptx::ld_shared_u16(src + t0.x); e[1] = ptx::ld_shared_u16(src + t0.y);
-                e[2] = ptx::ld_shared_u16(src + t0.z); e[3] = ptx::ld_shared_u16(src + t0.w);
-                e[4] = ptx::ld_shared_u16(src + t1.x); e[5] = ptx::ld_shared_u16(src + t1.y);
-                e[6] = ptx::ld_shared_u16(src + t1.z); e[7] = ptx::ld_shared_u16(src + t1.w);
-              } else {
-                const int tt[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+          const int nunits = ((len + 15) >> 4) * 2;  // 16-byte units the MMAs read (even)
+          const uint32_t stg = base + st.idx * a.stage_bytes + wst;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) e[j] = k0 + j < len ? ptx::ld_shared_u16(src + tt[j]) : 0u;
-              }
-              ptx::st_shared_v4(arow + (((uint32_t)uu ^ swz) << 4), e[0] | (e[1] << 16),
-                                e[2] | (e[3] << 16), e[4] | (e[5] << 16), e[6] | (e[7] << 16));
+          for (int h = 0; h < 2; ++h)
+            if (row_zero[h])
+              for (int uu = 0; uu < nunits; ++uu)
+                ptx::st_shared_v4(stg + roff[h] + (((uint32_t)uu ^ ((roff[h] >> 7) & 7u)) << 4), 0u, 0u, 0u, 0u);
+          // two units per step, their table entries shared by this thread's rows: the loads
+          // of both units and rows are independent and in flight together
+          const int* tk = tab + kin;
+#pragma unroll 1
+          for (int uu = 0; uu < nunits; uu += 2) {
+            const int k0 = 8 * uu;
+            const int4 t0 = *reinterpret_cast<const int4*>(tk + k0);
+            const int4 t1 = *reinterpret_cast<const int4*>(tk + k0 + 4);
+            const int4 t2 = *reinterpret_cast<const int4*>(tk + k0 + 8);
+            const int4 t3 = *reinterpret_cast<const int4*>(tk + k0 + 12);
+            const bool full = k0 + 16 <= len;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (h >= nrow || !row_ok[h]) continue;
+              const uint32_t src = pslot + 2u * (uint32_t)(rbase[h] + ao);
+              auto ld = [&](int off, int j) -> uint32_t {
+                return (full || k0 + j < len) ? ptx::ld_shared_u16(src + off) : 0u;
+              };
+              const uint32_t e0 = ld(t0.x, 0), e1 = ld(t0.y, 1), e2 = ld(t0.z, 2), e3 = ld(t0.w, 3);
+              const uint32_t e4 = ld(t1.x, 4), e5 = ld(t1.y, 5), e6 = ld(t1.z, 6), e7 = ld(t1.w, 7);
+              const uint32_t f0 = ld(t2.x, 8), f1 = ld(t2.y, 9), f2 = ld(t2.z, 10), f3 = ld(t2.w, 11);
+              const uint32_t f4 = ld(t3.x, 12), f5 = ld(t3.y, 13), f6 = ld(t3.z, 14), f7 = ld(t3.w, 15);
+              const uint32_t arow = stg + roff[h];
+              const uint32_t swz = (roff[h] >> 7) & 7u;
+              ptx::st_shared_v4(arow + (((uint32_t)uu ^ swz) << 4), e0 | (e1 << 16), e2 | (e3 << 16),
+                                e4 | (e5 << 16), e6 | (e7 << 16));
+              ptx::st_shared_v4(arow + (((uint32_t)(uu + 1) ^ swz) << 4), f0 | (f1 << 16),
+                                f2 | (f3 << 16), f4 | (f5 << 16), f6 | (f7 << 16));
             }
           }
           ptx::fence_proxy_async_smem();
