@@ -12,7 +12,7 @@ AUTO_PAD = {"NOTSET": 0, "SAME_UPPER": 1, "SAME_LOWER": 2, "VALID": 3}
 ACTIVATIONS = {None: 0, "Relu": 1, "LeakyRelu": 2, "Sigmoid": 3, "Tanh": 4, "HardSigmoid": 5,
                "HardSwish": 6, "Clip": 7, "QuickGelu": 8, "Elu": 9, "Gelu": 10, "FastGelu": 11,
                "Softplus": 12, "ThresholdedRelu": 13, "Erf": 14}
-ROUTES = {"auto": 0, "direct": 1, "igemm_tc": 2, "depthwise": 3}
+ROUTES = {"auto": 0, "direct": 1, "igemm_tc": 2, "depthwise": 3, "grouped": 4}
 ROUTE_NAMES = {v: k for k, v in ROUTES.items()}
 STATUS = {0: "OK", 1: "E_NULL", 2: "E_RANK", 3: "E_ATTR_LENGTH", 4: "E_ATTR_VALUE",
           5: "E_PADS_WITH_AUTOPAD", 6: "E_KERNEL_SHAPE", 7: "E_GROUP", 8: "E_BIAS_SHAPE",

@@ -223,16 +223,22 @@ fconv_status create(const fconv_desc* d, int device, const fconv_options* o, fco
   const fconv_route want = o ? o->route : FCONV_ROUTE_AUTO;
   fconv_route route = want;
   const int tile_n = (o && o->tile_n) ? o->tile_n : kDefaultPixelTile;
+  // groups of at most 16 input and 32 output channels move more bytes than they multiply:
+  // CUDA cores with a shared-memory halo box (2-D depthwise has a kernel of its own)
+  const bool small_groups = p->g.G > 1 && p->g.Cg <= 16 && p->g.Mg <= 32;
   if (want == FCONV_ROUTE_AUTO) {
     if (depthwise_supported(p->g)) route = FCONV_ROUTE_DEPTHWISE;
+    else if (small_groups && grouped_supported(p->g)) route = FCONV_ROUTE_GROUPED;
     else if (igemm_tc_supported(p->g, tile_n)) route = FCONV_ROUTE_IGEMM_TC;
     else route = FCONV_ROUTE_DIRECT;
   } else if (want == FCONV_ROUTE_DEPTHWISE && !depthwise_supported(p->g)) {
     st = FCONV_E_UNSUPPORTED;
+  } else if (want == FCONV_ROUTE_GROUPED && !grouped_supported(p->g)) {
+    st = FCONV_E_UNSUPPORTED;
   } else if (want == FCONV_ROUTE_IGEMM_TC && !igemm_tc_supported(p->g, tile_n)) {
     st = FCONV_E_UNSUPPORTED;
   } else if (want != FCONV_ROUTE_DIRECT && want != FCONV_ROUTE_DEPTHWISE &&
-             want != FCONV_ROUTE_IGEMM_TC) {
+             want != FCONV_ROUTE_IGEMM_TC && want != FCONV_ROUTE_GROUPED) {
     st = FCONV_E_UNSUPPORTED;
   }
   if (st == FCONV_OK && route == FCONV_ROUTE_IGEMM_TC && o && o->tile_n &&
@@ -342,6 +348,7 @@ fconv_status fconv_run(const fconv_plan* p, const void* x, const void* w, const 
   switch (p->route) {
     case FCONV_ROUTE_DIRECT: err = launch_direct(p->g, a, stream); break;
     case FCONV_ROUTE_DEPTHWISE: err = launch_depthwise(p->g, a, stream); break;
+    case FCONV_ROUTE_GROUPED: err = launch_grouped(p->g, a, stream); break;
     case FCONV_ROUTE_IGEMM_TC: err = launch_igemm_tc(p->g, p->igemm, a, stream); break;
     default: return FCONV_E_UNSUPPORTED;
   }

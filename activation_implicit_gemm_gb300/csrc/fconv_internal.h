@@ -57,6 +57,9 @@ struct IgemmConfig {
 int launch_direct(const ConvGeom& g, const ConvArgs& a, void* stream);
 int launch_depthwise(const ConvGeom& g, const ConvArgs& a, void* stream);
 bool depthwise_supported(const ConvGeom& g);
+int launch_grouped(const ConvGeom& g, const ConvArgs& a, void* stream);
+bool grouped_supported(const ConvGeom& g);
+int read_and_clear_grouped_error(void* stream, unsigned* value);
 
 // tcgen05 implicit GEMM: dispatch between the two A paths (k_igemm_tc.cu).
 int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, void* stream);

@@ -616,12 +616,14 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
 }
 
 int read_and_clear_device_error(void* stream, unsigned* value) {
-  unsigned v1 = 0, v2 = 0;
+  unsigned v1 = 0, v2 = 0, v3 = 0;
   int e = read_and_clear_tc_error((cudaStream_t)stream, &v1);
   if (e != 0) return e;
   e = read_and_clear_patch_error(stream, &v2);
   if (e != 0) return e;
-  *value = v1 | v2;
+  e = read_and_clear_grouped_error(stream, &v3);
+  if (e != 0) return e;
+  *value = v1 | v2 | v3;
   return 0;
 }
 

@@ -153,7 +153,8 @@ def main_kernel_name(case, route):
     C/group a multiple of 64; other tensor-core convs build A from the input patch)."""
     if route == "igemm_tc":
         return "igemm_tma_kernel" if case.w_shape[1] % 64 == 0 else "igemm_patch_kernel"
-    return {"depthwise": "dw_kernel_persistent", "direct": "direct_conv_kernel"}[route]
+    return {"depthwise": "dw_kernel_persistent", "direct": "direct_conv_kernel",
+            "grouped": "grouped_kernel"}[route]
 
 
 def run_ours(args):

@@ -104,7 +104,10 @@ typedef enum {
   FCONV_ROUTE_DIRECT = 1,   /* CUDA-core direct convolution: every dtype, rank, group */
   FCONV_ROUTE_IGEMM_TC = 2, /* tcgen05 implicit GEMM (float16): in-kernel im2col gather to
                                shared memory, accumulator in tensor memory, fused epilogue */
-  FCONV_ROUTE_DEPTHWISE = 3 /* CUDA-core depthwise 2-D kernel (C == M == group) */
+  FCONV_ROUTE_DEPTHWISE = 3, /* CUDA-core depthwise 2-D kernel (C == M == group) */
+  FCONV_ROUTE_GROUPED = 4    /* CUDA-core grouped conv with small groups (C/group <= 16,
+                                M/group <= 32), any rank: shared-memory halo box per (image,
+                                group, output box), f32 accumulation */
 } fconv_route;
 
 /* Operator inputs and attributes (manifest "inputs", "attributes"; README "Attributes").

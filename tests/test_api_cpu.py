@@ -139,6 +139,9 @@ def test_config_shapes_and_routes(lib):
             assert p.route == "direct"
         elif c.group == c.x_shape[1] and c.w_shape[1] == 1:
             assert p.route == "depthwise"
+        elif c.group > 1:
+            # small groups (C/group <= 16, M/group <= 32): CUDA cores, shared-memory halo box
+            assert p.route == "grouped"
         else:
             assert p.route == "igemm_tc"
             assert p.tile_n >= min(256, c.w_shape[0] // c.group)

@@ -189,10 +189,12 @@ ACTS = [(None, None), ("Relu", None), ("LeakyRelu", [0.01]), ("Sigmoid", None),
 
 
 @pytest.mark.parametrize("act,params", ACTS)
-@pytest.mark.parametrize("route", ["igemm_tc", "direct", "depthwise"])
+@pytest.mark.parametrize("route", ["igemm_tc", "direct", "depthwise", "grouped"])
 def test_activations(act, params, route):
     if route == "depthwise":
         xs, ws, extra = (2, 8, 13, 14), (8, 1, 3, 3), dict(group=8)
+    elif route == "grouped":
+        xs, ws, extra = (2, 16, 8, 10), (32, 4, 3, 3), dict(group=4)
     else:
         # 8x10 output: P % 8 == 0 takes the 16-byte Y/Z epilogue on the tensor-core route
         xs, ws, extra = (2, 16, 8, 10), (24, 16, 3, 3), dict()
@@ -225,6 +227,31 @@ def test_depthwise(idx, dtype):
     attrs = dict(attrs, group=C, activation="Clip", activation_params=[-1.0, 1.5])
     x, w, b, z = inputs(700 + idx, dtype, xs, (C, 1, k, k), True, True, attrs)
     compare(dtype, x, w, b, z, attrs, route="depthwise", what=f"dw {idx}")
+
+
+# ----------------------------------------------------------------------------- grouped (small groups)
+
+GROUPED_CASES = [
+    # (x_shape, w_shape, attrs): C/group <= 16, M/group in 1..32, every rank
+    ((2, 32, 16, 64, 64), (64, 8, 3, 3, 3), dict(group=4, strides=[2, 2, 2], auto_pad="SAME_LOWER")),
+    ((2, 12, 9, 10, 11), (24, 3, 3, 3, 3), dict(group=4, pads=[1, 1, 1, 1, 1, 1])),
+    ((2, 8, 7, 9, 8), (8, 1, 3, 3, 3), dict(group=8, pads=[1, 0, 1, 1, 2, 1])),       # 3-D depthwise
+    ((3, 16, 300), (16, 1, 7), dict(group=16, auto_pad="SAME_UPPER")),                  # 1-D depthwise
+    ((2, 32, 257), (64, 4, 5), dict(group=8, dilations=[2], pads=[4, 4])),
+    ((2, 6, 14, 15), (9, 2, 3, 3), dict(group=3, strides=[2, 1], dilations=[1, 2], pads=[1, 2, 0, 2])),
+    ((2, 64, 20, 19), (128, 16, 3, 3), dict(group=4, pads=[1, 1, 1, 1])),               # 16 -> 32
+    ((1, 10, 70, 90), (20, 5, 5, 5), dict(group=2, strides=[3, 2], pads=[2, 2, 2, 2])),  # several boxes
+    ((2, 8, 9, 9), (16, 1, 3, 3), dict(group=8, auto_pad="VALID")),                      # multiplier 2
+]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "f32"])
+@pytest.mark.parametrize("idx", range(len(GROUPED_CASES)))
+def test_grouped(idx, dtype):
+    xs, ws, attrs = GROUPED_CASES[idx]
+    attrs = dict(attrs, activation="HardSwish")
+    x, w, b, z = inputs(1600 + 10 * idx, dtype, xs, ws, True, idx % 2 == 0, attrs)
+    compare(dtype, x, w, b, z, attrs, route="grouped", what=f"grouped {idx}")
 
 
 # ----------------------------------------------------------------------------- direct fp32
@@ -296,6 +323,10 @@ EXACT_CASES = [
     ("f32", (2, 3, 5, 9, 8), (4, 3, 3, 3, 3), dict(strides=[1, 2, 1], auto_pad="SAME_UPPER"),
      "direct", {}, 2),
     ("f32", (2, 8, 14, 14), (8, 1, 3, 3), dict(group=8, pads=[1, 1, 1, 1]), "depthwise", {}, 2),
+    ("f16", (2, 12, 5, 9, 8), (24, 3, 3, 3, 3), dict(group=4, pads=[1, 1, 1, 1, 1, 1]), "grouped",
+     {}, 2),
+    ("f32", (2, 16, 40), (32, 4, 5), dict(group=4, strides=[2], auto_pad="SAME_LOWER"), "grouped",
+     {}, 2),
 ]
 
 
