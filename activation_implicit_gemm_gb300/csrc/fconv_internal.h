@@ -57,6 +57,7 @@ struct IgemmConfig {
 int launch_direct(const ConvGeom& g, const ConvArgs& a, void* stream);
 int launch_depthwise(const ConvGeom& g, const ConvArgs& a, void* stream);
 bool depthwise_supported(const ConvGeom& g);
+int read_and_clear_dw_error(void* stream, unsigned* value);
 int launch_grouped(const ConvGeom& g, const ConvArgs& a, void* stream);
 bool grouped_supported(const ConvGeom& g);
 int read_and_clear_grouped_error(void* stream, unsigned* value);

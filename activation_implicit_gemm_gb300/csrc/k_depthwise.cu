@@ -12,9 +12,9 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
-#include "epilogue.cuh"
-#include "fconv_internal.h"
-#include "ptx.cuh"
+#include <cstring>
+
+#include "tc_common.cuh"
 
 namespace fconv {
 
@@ -242,152 +242,385 @@ __global__ void __launch_bounds__(256) dw_kernel_block(ConvGeom g, const T* __re
 }
 
 
-// Persistent variant for planes that fit one tile (OH <= 64, OW <= 64) with stride 1,
-// dilation 1: a CTA loops over (image, channel) planes. The zero padding of the fp32
-// tile is written once (every plane has the same halo), the next plane's input rows are
-// loaded into registers while the current plane is computed, and each thread's Z values
-// are requested before its FMA loop so their latency hides behind it. The plane's
-// weights sit in shared memory (rows of 8 floats, read as broadcast vectors) rather than
-// in registers, so that more CTAs fit on an SM.
-template <typename T, int KH, int KW, int MAXV>
-__global__ void __launch_bounds__(256) dw_kernel_persistent(ConvGeom g, const T* __restrict__ x,
-                                                            const T* __restrict__ w,
-                                                            const T* __restrict__ b,
-                                                            const T* __restrict__ z,
-                                                            T* __restrict__ y, int TR, int TC,
-                                                            int pitch, long long planes) {
+// Tiled persistent path: stride 1 and dilation 1 on both axes, KH == KW == K known at
+// compile time, rows of X that TMA can address (16-byte multiples). The work is a list of
+// units (channel c, image n, output tile of THo x TWo), channel-major so that consecutive
+// units share their weights. A CTA takes a contiguous range of groups of PP units and
+// loops over it with a ring of NS shared-memory stages:
+//   - the load warp fills a stage NS groups ahead of the compute: the tile's receptive
+//     field of X (positions outside X filled with zeros by TMA, which is the zero padding)
+//     and the tile of Z;
+//   - thread (unit pp, column group cg, row strip) computes 4 consecutive outputs of TH
+//     consecutive rows. Each input row of its receptive field is read once from the box as
+//     16 values (f16: four 8-byte loads; f32: four 16-byte loads), converted to f32 and
+//     used for every output row it feeds: K x K x 4 x TH FMAs in f32 from K + 3 values per
+//     row. The weights stay in registers and are reloaded only when the unit's channel
+//     changes (a TMA store of Y from the stage, or weights staged per group, measured
+//     slower on the 56 x 56 x 7 x 7 stem shape);
+//   - bias seeds the accumulators; + Z, the activation and one rounding to T follow, and
+//     the 4 outputs of a row leave as one 8-byte (f16) or 16-byte (f32) store.
+// The box starts at the 16-byte boundary at or left of the tile's first input column, so
+// the first input column sits OFF = 0..3 elements into a thread's 16-value read; OFF is
+// the same for every tile (tiles are multiples of 8 columns wide) and selects one of four
+// compiled copies of the FMA block. Every wait is bounded in time; a wait that runs out
+// sets the device error word and the CTA leaves after the copies it issued have landed.
+constexpr int kDwTileThreads = 256;
+constexpr int kDwStages = 3;
+
+struct DwTileArgs {
+  int TWo, THo;           // output tile
+  int BW, BH;             // input box (elements)
+  int a_off;              // box column of the tile's first input column (ox0 - pW)
+  int ncg, nstrip, tpu;   // column groups, row strips and threads per unit
+  int PP;                 // units per group (computed together)
+  int tiles_w, tiles_h;
+  long long units, groups;
+  int z_tma;              // Z tile loaded by TMA (1) or read from global memory (0)
+  int vec_y;              // 4 outputs per row as one vector store (OW % 4 == 0)
+  uint32_t xbox_bytes, zbox_bytes;  // bytes of one input box and one Z tile
+  uint32_t z_off;         // the Z tile's offset in a unit's slot (128-byte aligned)
+  uint32_t unit_bytes, stage_bytes;
+  uint32_t bar_off;       // byte offset of the stage barriers
+};
+
+// The 16 values at a thread's read position in one box row, K + 3 of them (from OFF on)
+// converted to f32.
+template <typename T, int K, int OFF>
+__device__ __forceinline__ void dw_window(const T* row, float (&win)[K + 3]) {
+  constexpr int NQ = (OFF + K + 3 + 3) / 4;  // 4-element groups read
+  if constexpr (sizeof(T) == 2) {
+    uint2 q[NQ];
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) q[i] = reinterpret_cast<const uint2*>(row)[i];
+    const __half* h = reinterpret_cast<const __half*>(q);
+#pragma unroll
+    for (int i = 0; i < K + 3; ++i) win[i] = __half2float(h[i + OFF]);
+  } else {
+    float4 q[NQ];
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) q[i] = reinterpret_cast<const float4*>(row)[i];
+    const float* f = reinterpret_cast<const float*>(q);
+#pragma unroll
+    for (int i = 0; i < K + 3; ++i) win[i] = f[i + OFF];
+  }
+}
+
+// acc[o][j] += sum over (ky, kx) of W[ky][kx] * X[strip row o + ky][column j + kx]: every
+// box row of the strip's receptive field is read once and feeds up to K output rows.
+template <typename T, int K, int TH, int OFF>
+__device__ __forceinline__ void dw_strip(const T* box, int BW, const float (&wr)[K * K],
+                                         float (&acc)[TH][4]) {
+#pragma unroll
+  for (int r = 0; r < TH + K - 1; ++r) {
+    float win[K + 3];
+    dw_window<T, K, OFF>(box + r * BW, win);
+    // kx outer: consecutive FMAs update different accumulators (up to 4 x TH in flight)
+#pragma unroll
+    for (int kx = 0; kx < K; ++kx) {
+#pragma unroll
+      for (int o = 0; o < TH; ++o) {
+        const int ky = r - o;
+        if (ky < 0 || ky >= K) continue;
+        const float wv = wr[ky * K + kx];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[o][j] = fmaf(win[j + kx], wv, acc[o][j]);
+      }
+    }
+  }
+}
+
+// + Z, activation, rounding and the stores of a strip (rows past OH and columns past OW
+// are not stored).
+template <int ACT, typename T, int TH>
+__device__ __forceinline__ void dw_strip_store(const ConvGeom& g, const DwTileArgs& a,
+                                               const float (&acc)[TH][4], const T* zs, bool has_z,
+                                               const T* __restrict__ z, T* __restrict__ y,
+                                               long long obase, int oy, int ox) {
+  const int nv = min(4, g.OW - ox);
+#pragma unroll
+  for (int o = 0; o < TH; ++o) {
+    if (oy + o >= g.OH) break;
+    const T* zr = zs + o * a.TWo;
+    const long long orow = obase + (long long)(oy + o) * g.OW + ox;
+    float zv[4] = {0.f, 0.f, 0.f, 0.f};
+    if (has_z) {
+      if (a.z_tma) {
+        if constexpr (sizeof(T) == 2) {
+          const uint2 q = *reinterpret_cast<const uint2*>(zr);
+          const __half2 lo = *reinterpret_cast<const __half2*>(&q.x);
+          const __half2 hi = *reinterpret_cast<const __half2*>(&q.y);
+          zv[0] = __low2float(lo); zv[1] = __high2float(lo);
+          zv[2] = __low2float(hi); zv[3] = __high2float(hi);
+        } else {
+          const float4 q = *reinterpret_cast<const float4*>(zr);
+          zv[0] = q.x; zv[1] = q.y; zv[2] = q.z; zv[3] = q.w;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j < nv) zv[j] = to_f32(z[orow + j]);
+      }
+    }
+    float v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = act_eval<ACT, sizeof(T) == 2>(acc[o][j] + zv[j], g.alpha, g.beta);
+    if (a.vec_y && nv == 4) {
+      store4(y + orow, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (j < nv) y[orow + j] = from_f32<T>(v[j]);
+    }
+  }
+}
+
+// Unit u -> (channel, image, tile row, tile column).
+struct DwUnit {
+  int c, n, th, tw;
+};
+__device__ __forceinline__ DwUnit dw_unit(const DwTileArgs& a, int N, int u) {
+  const int tiles = a.tiles_w * a.tiles_h;
+  DwUnit r;
+  const int nt = N * tiles;
+  r.c = u / nt;
+  const int rem = u - r.c * nt;
+  r.n = rem / tiles;
+  const int t = rem - r.n * tiles;
+  r.th = t / a.tiles_w;
+  r.tw = t - r.th * a.tiles_w;
+  return r;
+}
+
+template <typename T, int K, int TH>
+__global__ void __launch_bounds__(kDwTileThreads, 2)
+    dw_tile_kernel(const ConvGeom g, const DwTileArgs a, const T* __restrict__ w,
+                   const T* __restrict__ b, const T* __restrict__ z, T* __restrict__ y,
+                   const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tz) {
+  extern __shared__ __align__(1024) uint8_t dsm[];
+  const uint32_t sbase = ptx::smem_addr(dsm);
+  const uint32_t full = sbase + a.bar_off;             // NS barriers: the stage is filled
+  const uint32_t empty = full + 8 * kDwStages;          // NS barriers: the compute warps are done
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(dsm + a.bar_off + 16 * kDwStages);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cwarps = (a.PP * a.tpu + 31) >> 5;          // compute warps; the next one loads
+  const int per = (int)((a.groups + gridDim.x - 1) / gridDim.x);
+  const int q0 = (int)blockIdx.x * per;
+  const int q1 = (int)min(a.groups, (long long)q0 + per);
+  if (tid == 0) {
+    for (int s = 0; s < kDwStages; ++s) {
+      ptx::mbar_init(full + 8 * s, 1);
+      ptx::mbar_init(empty + 8 * s, (uint32_t)cwarps);
+    }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
   ptx::pdl_wait();  // inputs may be the previous kernel's outputs
   ptx::pdl_trigger();
-  extern __shared__ float sx[];
-  constexpr int WIN = 4 + KW - 1;
-  constexpr int WV = (WIN + 3) / 4;
-  constexpr int VE = 16 / sizeof(T);
-  // rows of the tile: the last block row of threads reads up to row TR + KH - 2 (TR is OH
-  // rounded up to a multiple of 4); the weights follow the tile, KH rows of 8 floats
-  // Two such buffers alternate between planes: one barrier per plane, after which the
-  // threads compute from one buffer while the next plane is written into the other.
-  const int srows = TR + KH - 1;
-  const int bufsz = srows * pitch + KH * 8;
-  const int ixb = -g.pW - 4;                 // input column of tile column 0
-  const int nvr = g.IW / VE;                 // 16-byte vectors per input row
-  const int nvec = g.IH * nvr;               // per plane
-  for (int i = threadIdx.x * 4; i < 2 * bufsz; i += blockDim.x * 4)
-    *reinterpret_cast<float4*>(sx + i) = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int tcols = TC / 4;
-  const int ty = threadIdx.x / tcols, tx = threadIdx.x - ty * tcols;
-  const int oy = ty * 4, ox = tx * 4;
-  const bool active = oy < g.OH && ox < g.OW;
-  const int nv = active ? min(4, g.OW - ox) : 0, nr = active ? min(4, g.OH - oy) : 0;
 
-  uint4 pre[MAXV];
-  auto prefetch = [&](long long plane) {
-    const T* xp = x + plane * g.IS;
-#pragma unroll
-    for (int u = 0; u < MAXV; ++u) {
-      const int i = threadIdx.x + u * blockDim.x;
-      if (i < nvec) pre[u] = *reinterpret_cast<const uint4*>(xp + (long long)i * VE);
-    }
-  };
-  // the prefetched plane's weights and input rows into buffer buf (halo stays zero)
-  auto fill = [&](float* buf, long long pl) {
-    const int c = (int)(pl % g.C);
-    float* sw = buf + srows * pitch;
-    for (int i = threadIdx.x; i < KH * 8; i += blockDim.x) {
-      const int ky = i >> 3, kx = i & 7;
-      sw[i] = kx < KW ? to_f32(w[(long long)c * KH * KW + ky * KW + kx]) : 0.0f;
-    }
-#pragma unroll
-    for (int u = 0; u < MAXV; ++u) {
-      const int i = threadIdx.x + u * blockDim.x;
-      if (i < nvec) {
-        const int iy = i / nvr, c0 = (i - iy * nvr) * VE;
-        const T* e = reinterpret_cast<const T*>(&pre[u]);
-        float* d = buf + (iy + g.pH) * pitch + (c0 - ixb);
-#pragma unroll
-        for (int k = 0; k < VE; ++k) d[k] = to_f32(e[k]);
+  if (warp == cwarps) {
+    // ============================================================== load warp
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tx);
+      if (a.z_tma) ptx::prefetch_tmap(&tz);
+      int it = 0;
+      for (int q = q0; q < q1; ++q, ++it) {
+        const int s = it % kDwStages;
+        const uint32_t phase = (uint32_t)(it / kDwStages) & 1u;
+        if (!bounded_wait(empty + 8 * s, phase ^ 1u, abort_flag)) {
+          // what was issued lands before the CTA leaves
+          for (int k = 1; k < kDwStages && it - k >= 0; ++k)
+            drain_wait(full + 8 * ((it - k) % kDwStages), (uint32_t)((it - k) / kDwStages) & 1u);
+          break;
+        }
+        const uint32_t bar = full + 8 * s;
+        const int ubeg = q * a.PP;
+        const int nu = min(a.PP, (int)(a.units - ubeg));
+        ptx::mbar_arrive_expect_tx(bar, (uint32_t)nu * (a.xbox_bytes + (a.z_tma ? a.zbox_bytes : 0u)));
+        for (int pp = 0; pp < nu; ++pp) {
+          const DwUnit un = dw_unit(a, g.N, ubeg + pp);
+          const int plane = un.n * g.C + un.c;
+          const int ox0 = un.tw * a.TWo, oy0 = un.th * a.THo;
+          const uint32_t dst = sbase + (uint32_t)s * a.stage_bytes + (uint32_t)pp * a.unit_bytes;
+          ptx::tma_load_3d(dst, &tx, ox0 - g.pW - a.a_off, oy0 - g.pH, plane, bar);
+          if (a.z_tma) ptx::tma_load_3d(dst + a.z_off, &tz, ox0, oy0, plane, bar);
+        }
       }
     }
-  };
-  long long plane = blockIdx.x;
-  if (plane < planes) {
-    prefetch(plane);
-    __syncthreads();  // the zero fill of both buffers is complete
-    fill(sx, plane);
-    __syncthreads();
-    if (plane + gridDim.x < planes) prefetch(plane + gridDim.x);
+    return;
   }
-  for (int k = 0; plane < planes; plane += gridDim.x, k ^= 1) {
-    const float* cur = sx + k * bufsz;
-    const float* sw = cur + srows * pitch;
-    const int c = (int)(plane % g.C);
-    const float bias = b ? to_f32(b[c]) : 0.0f;
-    const long long obase = plane * g.P + (long long)oy * g.OW + ox;
-    // Z is requested before the FMAs and added after them, so its latency overlaps them
-    // (whole 4-wide runs: OW % 4 == 0 on this path, nv == 4)
-    uint2 zraw[4];  // the four rows' Z, as loaded (f16: 4 values; f32: converted below)
-    float4 zf[4];
+  if (warp > cwarps) return;
+
+  // ================================================================ compute warps
+  const int pp = tid / a.tpu, lt = tid - pp * a.tpu;
+  const int cg = lt % a.ncg, strip = lt / a.ncg;
+  const int off = a.a_off & 3;
+  int wc = -1;
+  float wr[K * K];
+  float bias = 0.0f;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      zraw[r] = make_uint2(0u, 0u);
-      zf[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (z && r < nr) {
-        if constexpr (sizeof(T) == 2) zraw[r] = *reinterpret_cast<const uint2*>(z + obase + (long long)r * g.OW);
-        else zf[r] = *reinterpret_cast<const float4*>(z + obase + (long long)r * g.OW);
+  for (int i = 0; i < K * K; ++i) wr[i] = 0.0f;
+  int it = 0;
+  for (int q = q0; q < q1; ++q, ++it) {
+    const int s = it % kDwStages;
+    const uint32_t phase = (uint32_t)(it / kDwStages) & 1u;
+    if (!bounded_wait(full + 8 * s, phase, abort_flag)) break;
+    const int u = q * a.PP + pp;
+    if (pp < a.PP && u < a.units) {
+      const DwUnit un = dw_unit(a, g.N, u);
+      const int ox = un.tw * a.TWo + 4 * cg, oy = un.th * a.THo + strip * TH;
+      if (ox < g.OW && oy < g.OH) {
+        if (un.c != wc) {
+          wc = un.c;
+#pragma unroll
+          for (int i = 0; i < K * K; ++i) wr[i] = to_f32(w[(long long)un.c * K * K + i]);
+          bias = b ? to_f32(b[un.c]) : 0.0f;
+        }
+        const uint8_t* unit = dsm + (size_t)s * a.stage_bytes + (size_t)pp * a.unit_bytes;
+        const T* xb = reinterpret_cast<const T*>(unit) + (strip * TH) * a.BW + 4 * cg + (a.a_off & ~3);
+        float acc[TH][4];
+#pragma unroll
+        for (int o = 0; o < TH; ++o)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[o][j] = bias;
+        switch (off) {
+          case 0: dw_strip<T, K, TH, 0>(xb, a.BW, wr, acc); break;
+          case 1: dw_strip<T, K, TH, 1>(xb, a.BW, wr, acc); break;
+          case 2: dw_strip<T, K, TH, 2>(xb, a.BW, wr, acc); break;
+          default: dw_strip<T, K, TH, 3>(xb, a.BW, wr, acc); break;
+        }
+        const T* zs = reinterpret_cast<const T*>(unit + a.z_off) + (strip * TH) * a.TWo + 4 * cg;
+        const long long obase = ((long long)un.n * g.C + un.c) * g.P;
+#define FCONV_DW_TILE_STORE(ACT) \
+  dw_strip_store<ACT, T, TH>(g, a, acc, zs, z != nullptr, z, y, obase, oy, ox)
+        FCONV_ACT_SWITCH(g.act, FCONV_DW_TILE_STORE)
+#undef FCONV_DW_TILE_STORE
       }
     }
-    if (active) {
-      float acc[4][4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[r][j] = bias;
-      const float* base = cur + oy * pitch + ox + 4;
-#pragma unroll
-      for (int ir = 0; ir < 4 + KH - 1; ++ir) {
-        float win[WV * 4];
-        const float4* rp = reinterpret_cast<const float4*>(base + ir * pitch);
-#pragma unroll
-        for (int q = 0; q < WV; ++q) {
-          const float4 f = rp[q];
-          win[4 * q] = f.x; win[4 * q + 1] = f.y; win[4 * q + 2] = f.z; win[4 * q + 3] = f.w;
-        }
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int ky = ir - r;
-          if (ky < 0 || ky >= KH) continue;
-          float wv[8];
-          const float4 w0 = *reinterpret_cast<const float4*>(sw + ky * 8);
-          const float4 w1 = *reinterpret_cast<const float4*>(sw + ky * 8 + 4);
-          wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
-          wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
-#pragma unroll
-          for (int kx = 0; kx < KW; ++kx)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[r][j] = fmaf(win[j + kx], wv[kx], acc[r][j]);
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        float zr[4];
-        if constexpr (sizeof(T) == 2) {
-          const __half2 a2 = *reinterpret_cast<const __half2*>(&zraw[r].x);
-          const __half2 b2 = *reinterpret_cast<const __half2*>(&zraw[r].y);
-          zr[0] = __low2float(a2); zr[1] = __high2float(a2); zr[2] = __low2float(b2); zr[3] = __high2float(b2);
-        } else {
-          zr[0] = zf[r].x; zr[1] = zf[r].y; zr[2] = zf[r].z; zr[3] = zf[r].w;
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[r][j] += zr[j];
-      }
-#define FCONV_DW_STORE(ACT) store_rows4<ACT, T>(acc, y, obase, g.OW, nr, g.alpha, g.beta)
-      FCONV_ACT_SWITCH(g.act, FCONV_DW_STORE)
-#undef FCONV_DW_STORE
-    }
-    const long long next = plane + gridDim.x;
-    if (next < planes) fill(sx + (k ^ 1) * bufsz, next);
-    __syncthreads();  // next plane staged; everyone is done with this plane's buffer
-    if (next + gridDim.x < planes) prefetch(next + gridDim.x);
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(empty + 8 * s);  // this warp is done with stage s
   }
+}
+
+struct DwTilePlan {
+  bool ok;
+  int TH;
+  DwTileArgs a;
+  size_t smem;
+};
+
+DwTilePlan dw_tile_plan(const ConvGeom& g) {
+  DwTilePlan p{};
+  p.ok = false;
+  const int K = g.KW;
+  if (!(g.Cg == 1 && g.Mg == 1 && g.KD == 1 && g.ID == 1 && g.OD == 1)) return p;
+  if (!(g.sW == 1 && g.dW == 1 && g.sH == 1 && g.dH == 1 && g.KH == K)) return p;
+  if (K != 3 && K != 5 && K != 7) return p;
+  const int es = g.dtype == FCONV_F16 ? 2 : 4;
+  const int xal = 16 / es;
+  if ((g.IW * es) % 16 != 0) return p;  // rows of X must be TMA-addressable
+  DwTileArgs& a = p.a;
+  a.TWo = imin(64, (g.OW + 7) / 8 * 8);
+  a.a_off = ((-g.pW) % xal + xal) % xal;
+  a.BW = (a.TWo + (a.a_off & ~3) + 12 + xal - 1) / xal * xal;
+  a.ncg = a.TWo / 4;
+  a.tiles_w = (g.OW + a.TWo - 1) / a.TWo;
+  // rows per thread and units per group: the fewest issued FMA and load instructions,
+  // counting the idle lanes of partly filled warps and the rows past OH
+  double best = 0.0;
+  const int ths[3] = {8, 7, 4};
+  for (int th : ths) {
+    const int tho = imin((g.OH + th - 1) / th * th, (64 / th) * th);
+    const int nstrip = tho / th;
+    const int tpu = a.ncg * nstrip;
+    if (tpu > kDwTileThreads - 32) continue;
+    const long long units = (long long)g.N * g.C * ((g.OH + tho - 1) / tho) * a.tiles_w;
+    for (int pp = 1; (pp * tpu + 31) / 32 * 32 + 32 <= kDwTileThreads && pp <= 8; ++pp) {
+      const long long warps = (pp * tpu + 31) / 32;
+      const double cost = (double)((units + pp - 1) / pp) * (double)warps *
+                          (double)(th * K * K * 4 + (th + K - 1) * 8);
+      if (!p.ok || cost < best) {
+        best = cost;
+        p.ok = true;
+        p.TH = th;
+        a.THo = tho;
+        a.nstrip = nstrip;
+        a.tpu = tpu;
+        a.PP = pp;
+        a.units = units;
+      }
+    }
+  }
+  if (!p.ok) return p;
+  a.tiles_h = (g.OH + a.THo - 1) / a.THo;
+  a.groups = (a.units + a.PP - 1) / a.PP;
+  a.BH = a.THo + K - 1;
+  a.z_tma = (g.OW * es) % 16 == 0 ? 1 : 0;
+  a.vec_y = g.OW % 4 == 0 ? 1 : 0;
+  a.xbox_bytes = (uint32_t)(a.BW * a.BH * es);
+  a.zbox_bytes = (uint32_t)(a.TWo * a.THo * es);
+  // a unit's slot: the input box, then the Z tile
+  a.z_off = (a.xbox_bytes + 127u) & ~127u;
+  a.unit_bytes = a.z_off + (a.z_tma ? (a.zbox_bytes + 127u) & ~127u : 0u);
+  a.stage_bytes = (uint32_t)a.PP * a.unit_bytes;
+  a.bar_off = (uint32_t)kDwStages * a.stage_bytes;
+  p.smem = (size_t)a.bar_off + 16 * kDwStages + 16;
+  if (p.smem > 200 * 1024 || a.units > 0x7fffffffLL) p.ok = false;
+  return p;
+}
+
+template <typename T>
+int launch_dw_tile(const ConvGeom& g, const DwTilePlan& p, const ConvArgs& args, cudaStream_t s) {
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc) return (int)cudaErrorNotSupported;
+  const DwTileArgs& a = p.a;
+  const cuuint64_t es = sizeof(T);
+  const CUtensorMapDataType dt = sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const cuuint32_t est[3] = {1, 1, 1};
+  CUtensorMap tx, tz;
+  std::memset(&tx, 0, sizeof(tx));
+  std::memset(&tz, 0, sizeof(tz));
+  auto encode = [&](CUtensorMap* m, const void* ptr, cuuint64_t d0, cuuint64_t d1, cuuint32_t b0,
+                    cuuint32_t b1) {
+    const cuuint64_t dims[3] = {d0, d1, (cuuint64_t)g.N * g.C};
+    const cuuint64_t str[2] = {d0 * es, d0 * d1 * es};
+    const cuuint32_t box[3] = {b0, b1, 1};
+    return enc(m, dt, 3, const_cast<void*>(ptr), dims, str, box, est, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  if (!encode(&tx, args.x, (cuuint64_t)g.IW, (cuuint64_t)g.IH, (cuuint32_t)a.BW, (cuuint32_t)a.BH))
+    return (int)cudaErrorInvalidValue;
+  DwTileArgs aa = a;
+  if (aa.z_tma && args.z) {
+    if (!encode(&tz, args.z, (cuuint64_t)g.OW, (cuuint64_t)g.OH, (cuuint32_t)a.TWo, (cuuint32_t)a.THo))
+      return (int)cudaErrorInvalidValue;
+  } else {
+    aa.z_tma = 0;  // nothing to load
+  }
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int threads = (a.PP * a.tpu + 31) / 32 * 32 + 32;  // compute warps + the load warp
+#define FCONV_DW_TILE(KV, THV)                                                                  \
+  if (g.KW == KV && p.TH == THV) {                                                              \
+    auto k = dw_tile_kernel<T, KV, THV>;                                                        \
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,         \
+                                         (int)p.smem);                                          \
+    if (e != cudaSuccess) return (int)e;                                                        \
+    int per_sm = 1;                                                                             \
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, p.smem);                 \
+    long long grid = (long long)sms * (per_sm > 0 ? per_sm : 1);                                \
+    if (grid > a.groups) grid = a.groups;                                                       \
+    if (g.max_ctas > 0 && grid > g.max_ctas) grid = g.max_ctas;                                 \
+    return launch_pdl(k, dim3((unsigned)grid), dim3(threads), p.smem, s, g, aa,                 \
+                      (const T*)args.w, (const T*)args.b, (const T*)args.z, (T*)args.y, tx, tz); \
+  }
+  FCONV_DW_TILE(3, 8) FCONV_DW_TILE(3, 7) FCONV_DW_TILE(3, 4)
+  FCONV_DW_TILE(5, 8) FCONV_DW_TILE(5, 7) FCONV_DW_TILE(5, 4)
+  FCONV_DW_TILE(7, 8) FCONV_DW_TILE(7, 7) FCONV_DW_TILE(7, 4)
+#undef FCONV_DW_TILE
+  return (int)cudaErrorInvalidValue;
 }
 
 // General path: any stride and dilation, one output per thread iteration.
@@ -441,37 +674,9 @@ int launch_dw_t(const ConvGeom& g, const ConvArgs& a, cudaStream_t s) {
   const T* z = (const T*)a.z;
   T* y = (T*)a.y;
   const bool unit = g.sW == 1 && g.dW == 1 && g.sH == 1 && g.dH == 1;
-  constexpr int VE = 16 / sizeof(T);
-  if (unit && g.KH == g.KW && (g.KW == 3 || g.KW == 5 || g.KW == 7) && g.OH <= 64 &&
-      g.OW <= 64 && g.OW % 4 == 0 && g.IW % VE == 0 && g.IS % VE == 0 &&
-      (long long)g.IH * (g.IW / VE) <= 4LL * ((g.OW + 3) / 4) * ((g.OH + 3) / 4) &&
-      g.IH + g.pH <= g.OH + g.KH - 1 && g.IW + g.pW + 4 <= (g.OW + 3) / 4 * 4 + 4 + g.KW + 3) {
-    // persistent CTAs; the whole plane is one tile
-    const int TC = (g.OW + 3) / 4 * 4;
-    const int TR = (g.OH + 3) / 4 * 4;
-    const int threads = (TC / 4) * (TR / 4);
-    const int pitch = (TC + 4 + g.KW + 3 + 3) / 4 * 4 + 4;
-    const size_t smem = 2 * ((size_t)(TR + g.KH - 1) * pitch + (size_t)g.KH * 8) * sizeof(float);
-    const long long planes = (long long)g.N * g.C;
-    int dev = 0, sms = 152;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-#define FCONV_DW_PERSIST(KV)                                                                    \
-  if (g.KW == KV) {                                                                             \
-    auto k = dw_kernel_persistent<T, KV, KV, 4>;                                                \
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);           \
-    int per_sm = 1;                                                                             \
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem);                  \
-    long long grid = (long long)sms * (per_sm > 0 ? per_sm : 1);                                \
-    if (grid > planes) grid = planes;                                                           \
-    if (g.max_ctas > 0 && grid > g.max_ctas) grid = g.max_ctas;                                 \
-    return launch_pdl(k, dim3((unsigned)grid), dim3(threads), smem, s, g, x, w, b, z, y, TR, TC, \
-                      pitch, planes);                                                           \
-  }
-    FCONV_DW_PERSIST(3)
-    FCONV_DW_PERSIST(5)
-    FCONV_DW_PERSIST(7)
-#undef FCONV_DW_PERSIST
+  {
+    const DwTilePlan tp = dw_tile_plan(g);
+    if (tp.ok) return launch_dw_tile<T>(g, tp, a, s);
   }
   if (unit && g.KH == g.KW && (g.KW == 3 || g.KW == 5 || g.KW == 7)) {
     // output tile: TC columns (<= 64, a multiple of 4), TR rows, at most 256 threads
@@ -508,6 +713,10 @@ bool depthwise_supported(const ConvGeom& g) {
   const long long blocks = (long long)g.N * g.C * dw_shape(g).bands;
   if (blocks > 0x7fffffffLL) return false;
   return dw_shape(g).smem <= (size_t)kDwMaxSmem;
+}
+
+int read_and_clear_dw_error(void* stream, unsigned* value) {
+  return read_and_clear_tc_error((cudaStream_t)stream, value);
 }
 
 int launch_depthwise(const ConvGeom& g, const ConvArgs& a, void* stream) {

@@ -616,14 +616,16 @@ int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, 
 }
 
 int read_and_clear_device_error(void* stream, unsigned* value) {
-  unsigned v1 = 0, v2 = 0, v3 = 0;
+  unsigned v1 = 0, v2 = 0, v3 = 0, v4 = 0;
   int e = read_and_clear_tc_error((cudaStream_t)stream, &v1);
   if (e != 0) return e;
   e = read_and_clear_patch_error(stream, &v2);
   if (e != 0) return e;
   e = read_and_clear_grouped_error(stream, &v3);
   if (e != 0) return e;
-  *value = v1 | v2 | v3;
+  e = read_and_clear_dw_error(stream, &v4);
+  if (e != 0) return e;
+  *value = v1 | v2 | v3 | v4;
   return 0;
 }
 

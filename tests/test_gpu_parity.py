@@ -216,6 +216,13 @@ DW_CASES = [
     ((3, 16, 24, 32), 3, dict(pads=[1, 1, 1, 1])),    # persistent: one tile per plane
     ((2, 8, 56, 56), 7, dict(pads=[3, 3, 3, 3])),     # persistent, the stem's geometry
     ((2, 4, 8, 8), 5, dict(pads=[2, 2, 2, 2])),
+    # tiled path: several tiles per plane in both directions, each left pad (it sets where
+    # a thread's 16-value read starts), widths that are not multiples of 4 or 8
+    ((2, 6, 70, 72), 5, dict(pads=[2, 1, 2, 3])),
+    ((3, 5, 33, 40), 3, dict(pads=[0, 2, 1, 0])),
+    ((2, 4, 19, 24), 7, dict(pads=[3, 0, 3, 0])),
+    ((1, 3, 64, 136), 7, dict(auto_pad="SAME_UPPER")),
+    ((2, 3, 12, 16), 3, dict(pads=[1, 3, 0, 3])),
 ]
 
 
