@@ -223,9 +223,12 @@ fconv_status create(const fconv_desc* d, int device, const fconv_options* o, fco
   const fconv_route want = o ? o->route : FCONV_ROUTE_AUTO;
   fconv_route route = want;
   const int tile_n = (o && o->tile_n) ? o->tile_n : kDefaultPixelTile;
-  // groups of at most 16 input and 32 output channels move more bytes than they multiply:
-  // CUDA cores with a shared-memory halo box (2-D depthwise has a kernel of its own)
-  const bool small_groups = p->g.G > 1 && p->g.Cg <= 16 && p->g.Mg <= 32;
+  // groups with few channels and short reductions (C/group * kernel <= 64, e.g. 1-D and 3-D
+  // depthwise) do few FMAs per output: CUDA cores with a shared-memory halo box (2-D
+  // depthwise has a kernel of its own). Longer group reductions go to the tensor cores,
+  // which were faster on the 3-D grouped conv X[2,32,16,64,64] W[64,8,3,3,3] group 4
+  // (C/group * kernel = 216).
+  const bool small_groups = p->g.G > 1 && p->g.Cg <= 16 && p->g.Mg <= 32 && p->g.Kg <= 64;
   if (want == FCONV_ROUTE_AUTO) {
     if (depthwise_supported(p->g)) route = FCONV_ROUTE_DEPTHWISE;
     else if (small_groups && grouped_supported(p->g)) route = FCONV_ROUTE_GROUPED;

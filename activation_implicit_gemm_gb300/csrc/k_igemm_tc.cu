@@ -249,12 +249,22 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 
 // X (N, C, spatial S) -> Xb[c/64][n][s][64]. Block (x, cb) moves 64 channels of the
 // flattened positions q = n*S + s in [128x, 128x + 128), across image boundaries when S is
-// small: four 16-byte loads per thread (8 positions of one channel), all in flight, into a
-// shared tile, then four 16-byte stores per thread (8 channels of one position). Needs
-// S % 8 == 0 (a load never straddles two images) and N*S < 2^31 (32-bit position
-// decoding); otherwise pack_x_scalar is used.
-constexpr int kPackPitch = 138;  // halves per channel row: 16-byte rows, few bank conflicts
+// small. In: four 16-byte loads per thread (8 positions of one channel), all in flight,
+// each stored as one 16-byte chunk of a channel row of the shared tile; chunk k of channel
+// c sits at k ^ ((c / 8) % 8). Out: a thread takes two adjacent positions and 8 channels
+// (lanes: the 8 channel groups of 4 position pairs): eight 32-bit loads, byte permutes
+// that pair up the channels, and one 16-byte store per position, so a warp writes whole
+// 128-byte rows of Xb; the chunk swizzle puts the 8 channel groups of a load on distinct
+// banks. Needs S % 8 == 0 (a load never straddles two images) and N*S < 2^31 (32-bit
+// position decoding); otherwise pack_x_scalar is used.
+constexpr int kPackPitch = 136;  // halves per channel row (272 bytes, 16-byte aligned)
 constexpr size_t kPackSmem = 64 * kPackPitch * 2;
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
 
 __device__ __forceinline__ void pack_x_block(const uint16_t* __restrict__ x, uint16_t* __restrict__ xb,
                                              int N, int C, long long S, long long bx, int cb,
@@ -278,22 +288,29 @@ __device__ __forceinline__ void pack_x_block(const uint16_t* __restrict__ x, uin
   for (int i = 0; i < 4; ++i) {
     const int v = threadIdx.x + 256 * i;
     const int c = v >> 4, pv = v & 15;
-    uint32_t* d = reinterpret_cast<uint32_t*>(t + c * kPackPitch + pv * 8);  // 4-byte aligned
-    d[0] = buf[i].x; d[1] = buf[i].y; d[2] = buf[i].z; d[3] = buf[i].w;
+    *reinterpret_cast<uint4*>(t + c * kPackPitch + ((pv ^ ((c >> 3) & 7)) * 8)) = buf[i];
   }
   __syncthreads();
   uint16_t* dst = xb + ((long long)cb * NS + q0) * 64;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int o = threadIdx.x + 256 * i;
-    const int p = o >> 3, part = o & 7;
+  for (int i = 0; i < 2; ++i) {
+    const int item = threadIdx.x + 256 * i;
+    const int part = item & 7, pp = item >> 3;  // channels 8*part.., positions 2pp, 2pp+1
+    const int p = 2 * pp;
     if (p >= rows) continue;
-    uint32_t w[4];
+    const int sw = (((p >> 3) ^ part) << 3) + (p & 7);  // swizzled place of position p
+    uint32_t wv[8];
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      w[e] = (uint32_t)t[(8 * part + 2 * e) * kPackPitch + p] |
-             ((uint32_t)t[(8 * part + 2 * e + 1) * kPackPitch + p] << 16);
-    *reinterpret_cast<uint4*>(dst + (long long)p * 64 + 8 * part) = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int j = 0; j < 8; ++j)
+      wv[j] = *reinterpret_cast<const uint32_t*>(t + (8 * part + j) * kPackPitch + sw);
+    uint32_t lo[4], hi[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      lo[e] = prmt(wv[2 * e], wv[2 * e + 1], 0x5410u);  // channels 2e, 2e+1 at position p
+      hi[e] = prmt(wv[2 * e], wv[2 * e + 1], 0x7632u);  // the same at position p + 1
+    }
+    *reinterpret_cast<uint4*>(dst + (long long)p * 64 + 8 * part) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    *reinterpret_cast<uint4*>(dst + (long long)(p + 1) * 64 + 8 * part) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
   }
 }
 

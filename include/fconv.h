@@ -107,7 +107,8 @@ typedef enum {
   FCONV_ROUTE_DEPTHWISE = 3, /* CUDA-core depthwise 2-D kernel (C == M == group) */
   FCONV_ROUTE_GROUPED = 4    /* CUDA-core grouped conv with small groups (C/group <= 16,
                                 M/group <= 32), any rank: shared-memory halo box per (image,
-                                group, output box), f32 accumulation */
+                                group, output box), f32 accumulation. The planner picks it
+                                when also C/group * prod(kernel) <= 64. */
 } fconv_route;
 
 /* Operator inputs and attributes (manifest "inputs", "attributes"; README "Attributes").

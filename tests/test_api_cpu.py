@@ -139,8 +139,8 @@ def test_config_shapes_and_routes(lib):
             assert p.route == "direct"
         elif c.group == c.x_shape[1] and c.w_shape[1] == 1:
             assert p.route == "depthwise"
-        elif c.group > 1:
-            # small groups (C/group <= 16, M/group <= 32): CUDA cores, shared-memory halo box
+        elif c.group > 1 and np.prod(c.w_shape[1:]) <= 64:
+            # small groups with short reductions: CUDA cores, shared-memory halo box
             assert p.route == "grouped"
         else:
             assert p.route == "igemm_tc"
