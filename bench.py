@@ -40,12 +40,22 @@ METRIC = "FusedConv TFLOP/s (fp16/fp32) and % of roofline per config; depthwise 
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+# CUDA-core f32 FMA peak of a GB300: 152 SMs x 128 FMA lanes x 2 FLOP per FMA x the
+# maximum SM clock (2070 MHz) = 80.5 TFLOP/s. The depthwise, grouped and direct routes
+# compute on these lanes, so their compute roofline is this one, not the tensor cores'.
+SMS, FMA_LANES_PER_SM, SM_MAX_MHZ = 152, 128, 2070.0
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
-        d = json.load(open(p))
-        return d, "measured"
-    return PEAKS_FALLBACK, "fallback"
+        d = dict(json.load(open(p)))
+        kind = "measured"
+    else:
+        d, kind = dict(PEAKS_FALLBACK), "fallback"
+    mhz = float(d.get("sm_max_mhz", SM_MAX_MHZ))
+    d["alu_f32_tflops"] = SMS * FMA_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+    return d, kind
 
 
 def dist_env():
@@ -143,9 +153,21 @@ def oracle_tensors(case):
     return workloads.make_inputs(case, ys), ys
 
 
-def bound_of(flops, bytes_, peaks):
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    return "tensor" if flops / bytes_ >= ridge else "hbm"
+CUDA_CORE_ROUTES = ("depthwise", "grouped", "direct")
+
+
+def bound_of(flops, bytes_, peaks, route="igemm_tc"):
+    """The roofline a launch sits under: its compute units' peak (tensor cores, or the f32
+    FMA lanes for the CUDA-core routes) against the measured HBM copy rate."""
+    comp = peaks["alu_f32_tflops"] if route in CUDA_CORE_ROUTES else peaks["bf16_tflops"]
+    ridge = comp * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if flops / bytes_ < ridge:
+        return "hbm"
+    return "alu" if route in CUDA_CORE_ROUTES else "tensor"
+
+
+def compute_peak(bound, peaks):
+    return peaks["alu_f32_tflops"] if bound == "alu" else peaks["bf16_tflops"]
 
 
 def main_kernel_name(case, route):
@@ -153,7 +175,7 @@ def main_kernel_name(case, route):
     C/group a multiple of 64; other tensor-core convs build A from the input patch)."""
     if route == "igemm_tc":
         return "igemm_tma_kernel" if case.w_shape[1] % 64 == 0 else "igemm_patch_kernel"
-    return {"depthwise": "dw_kernel_persistent", "direct": "direct_conv_kernel",
+    return {"depthwise": "dw_tile_kernel", "direct": "direct_conv_kernel",
             "grouped": "grouped_kernel"}[route]
 
 
@@ -258,14 +280,15 @@ def run_ours(args):
         p = c["plan"]
         ms = per_conv_ms[i] / Kc
         fl, by = p.flops, p.bytes
-        bnd = bound_of(fl, by, peaks)
+        bnd = bound_of(fl, by, peaks, p.route)
         tf = fl / (ms * 1e-3) / 1e12
         gbs = by / (ms * 1e-3) / 1e9
-        if bnd == "tensor":
-            frac = tf / peaks["bf16_tflops"]
+        if bnd in ("tensor", "alu"):
+            frac = tf / compute_peak(bnd, peaks)
         else:
             frac = gbs / peaks["hbm_gbs"]
-        attain = min(peaks["bf16_tflops"] * 1e12, fl / by * peaks["hbm_gbs"] * 1e9) / 1e12
+        comp = peaks["alu_f32_tflops"] if p.route in CUDA_CORE_ROUTES else peaks["bf16_tflops"]
+        attain = min(comp * 1e12, fl / by * peaks["hbm_gbs"] * 1e9) / 1e12
         per.append({"conv": c["case"].name, "route": p.route, "tile_n": p.tile_n,
                     "split_k": p.split_k, "us": round(ms * 1e3, 2), "tflops": round(tf, 2),
                     "gbs": round(gbs, 1), "bound": bnd, "frac_of_bound": round(frac, 4),
@@ -274,16 +297,18 @@ def run_ours(args):
     top = max(range(len(convs)), key=lambda i: per_conv_ms[i])
     tp = convs[top]["plan"]
     tms = per_conv_ms[top] / Kc
-    tb = bound_of(tp.flops, tp.bytes, peaks)
-    if tb == "tensor":
-        ach, pk, unit = tp.flops / (tms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    tb = bound_of(tp.flops, tp.bytes, peaks, tp.route)
+    if tb in ("tensor", "alu"):
+        ach, pk, unit = tp.flops / (tms * 1e-3) / 1e12, compute_peak(tb, peaks), "TFLOP/s"
     else:
         ach, pk, unit = tp.bytes / (tms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
     traffic = load_traffic(convs[top]["case"].name)
     roofline = {"bound": tb, "achieved": round(ach, 3), "peak": pk, "unit": unit,
                 "frac": round(ach / pk, 4), "traffic": traffic,
                 "kernel": main_kernel_name(convs[top]["case"], tp.route),
-                "launch": convs[top]["case"].name, "peak_kind": f"{peaks_kind} (burst)",
+                "launch": convs[top]["case"].name,
+                "peak_kind": ("derived: 152 SMs x 128 f32 FMA lanes x 2 FLOP x max SM clock"
+                              if tb == "alu" else f"{peaks_kind} (burst)"),
                 "algorithmic_flops_per_launch": tp.flops,
                 "algorithmic_bytes_per_launch": tp.bytes}
 
