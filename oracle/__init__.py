@@ -45,6 +45,24 @@ class _Attrs(ctypes.Structure):
                 ("act_params", ctypes.c_double * 2)]
 
 
+class _TAttrs(ctypes.Structure):
+    _fields_ = [("rank", ctypes.c_int),
+                ("x_shape", ctypes.c_int64 * 5),
+                ("w_shape", ctypes.c_int64 * 5),
+                ("group", ctypes.c_int64),
+                ("n_strides", ctypes.c_int),
+                ("n_dilations", ctypes.c_int),
+                ("n_pads", ctypes.c_int),
+                ("n_output_padding", ctypes.c_int),
+                ("strides", ctypes.c_int64 * 3),
+                ("dilations", ctypes.c_int64 * 3),
+                ("pads", ctypes.c_int64 * 6),
+                ("output_padding", ctypes.c_int64 * 3),
+                ("activation", ctypes.c_int),
+                ("n_act_params", ctypes.c_int),
+                ("act_params", ctypes.c_double * 2)]
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (OpenMP) unless an up-to-date library exists."""
     if (not force and os.path.exists(_LIB)
@@ -74,6 +92,10 @@ def lib():
                                            ctypes.c_double]
         _lib.oracle_activation.restype = ctypes.c_double
         _lib.oracle_max_threads.restype = ctypes.c_int
+        _lib.oracle_transpose_output_shape.argtypes = [P(_TAttrs), P(ctypes.c_int64)]
+        _lib.oracle_transpose_output_shape.restype = ctypes.c_int
+        _lib.oracle_conv_transpose.argtypes = [P(_TAttrs)] + [ctypes.c_void_p] * 6 + [ctypes.c_int]
+        _lib.oracle_conv_transpose.restype = ctypes.c_int
     return _lib
 
 
@@ -161,6 +183,86 @@ def fused_conv(x: np.ndarray, w: np.ndarray, b: Optional[np.ndarray] = None,
 
     st = lib().oracle_fused_conv(ctypes.byref(a), ptr(xd), ptr(wd), ptr(bd), ptr(zd), ptr(y),
                                  ptr(s), int(nthreads))
+    if st != 0:
+        raise ValueError(f"oracle failed: {STATUS[st]}")
+    return y, s
+
+
+def make_tattrs(x_shape, w_shape, group: int = 1, strides=None, dilations=None, pads=None,
+                output_padding=None, activation: Optional[str] = None,
+                activation_params=None) -> _TAttrs:
+    a = _TAttrs()
+    a.rank = len(x_shape)
+    if len(w_shape) != len(x_shape) or not 3 <= len(x_shape) <= 5:
+        a.rank = 0
+    for i, v in enumerate(list(x_shape)[:5]):
+        a.x_shape[i] = int(v)
+    for i, v in enumerate(list(w_shape)[:5]):
+        a.w_shape[i] = int(v)
+    a.group = int(group)
+
+    def put(arr, vals, cap):
+        if vals is None:
+            return 0
+        vals = list(vals)
+        for i, v in enumerate(vals[:cap]):
+            arr[i] = int(v)
+        return len(vals) if len(vals) <= cap else cap + 1
+
+    a.n_strides = put(a.strides, strides, 3)
+    a.n_dilations = put(a.dilations, dilations, 3)
+    a.n_pads = put(a.pads, pads, 6)
+    a.n_output_padding = put(a.output_padding, output_padding, 3)
+    a.activation = act_id(activation)
+    if activation_params is None:
+        a.n_act_params = -1
+    else:
+        ap = list(activation_params)
+        a.n_act_params = len(ap)
+        for i, v in enumerate(ap[:2]):
+            a.act_params[i] = float(v)
+    return a
+
+
+def transpose_resolve(x_shape, w_shape, **attrs):
+    """(status name, y_shape) of a transposed convolution."""
+    a = make_tattrs(x_shape, w_shape, **attrs)
+    ys = (ctypes.c_int64 * 5)()
+    st = lib().oracle_transpose_output_shape(ctypes.byref(a), ys)
+    if st != 0:
+        return STATUS[st], None
+    return "OK", tuple(ys[i] for i in range(len(x_shape)))
+
+
+def transpose_output_shape(x_shape, w_shape, **attrs):
+    st, ys = transpose_resolve(x_shape, w_shape, **attrs)
+    if st != "OK":
+        raise ValueError(f"oracle rejects the attributes: {st}")
+    return ys
+
+
+def conv_transpose(x: np.ndarray, w: np.ndarray, b: Optional[np.ndarray] = None,
+                   z: Optional[np.ndarray] = None, nthreads: int = 0, **attrs):
+    """Transposed convolution with the fused epilogue: Y (float64, unrounded) and
+    sum |x*w| per output, from dtype-rounded inputs. W is (C, M/group, kernel...)."""
+    ys = transpose_output_shape(x.shape, w.shape, **attrs)
+    a = make_tattrs(x.shape, w.shape, **attrs)
+    xd = np.ascontiguousarray(x, dtype=np.float64)
+    wd = np.ascontiguousarray(w, dtype=np.float64)
+    bd = None if b is None else np.ascontiguousarray(b, dtype=np.float64)
+    zd = None if z is None else np.ascontiguousarray(z, dtype=np.float64)
+    if bd is not None and bd.shape != (ys[1],):
+        raise ValueError("bias must be rank 1 with length M")
+    if zd is not None and zd.shape != tuple(ys):
+        raise ValueError("Z must have the shape of Y")
+    y = np.empty(ys, dtype=np.float64)
+    s = np.empty(ys, dtype=np.float64)
+
+    def ptr(arr):
+        return None if arr is None else arr.ctypes.data_as(ctypes.c_void_p)
+
+    st = lib().oracle_conv_transpose(ctypes.byref(a), ptr(xd), ptr(wd), ptr(bd), ptr(zd),
+                                     ptr(y), ptr(s), int(nthreads))
     if st != 0:
         raise ValueError(f"oracle failed: {STATUS[st]}")
     return y, s

@@ -21,9 +21,18 @@
  *    (#20873, "on-the-fly sampling ... zero when out of range") and the manifest's
  *    params_ncdhw3d block (padD/padH/padW = effectivePad*) describe.
  *
+ * Transposed convolution (oracle_conv_transpose): ExecuTorch WebGPU PR #20849, the
+ * transposed form of aten.convolution.default ("conv_transpose2d.wgsl ... gather-form
+ * transposed conv", weight "in the un-flipped torch transposed layout [IC, OC/groups, KH,
+ * KW]", "output_padding >= stride" rejected). The oracle writes the definition in its
+ * scatter form: every input element adds x * w to the output at
+ * input*stride - pad_begin + tap*dilation.
+ *
  * Parity is pinned by the tests against PyTorch CPU float64 convolutions (a library
  * routine), brute force on tiny inputs, 1x1 conv == matmul, the delta kernel,
- * rank embedding, closed-form activation values and the output-size formulas.
+ * rank embedding, closed-form activation values and the output-size formulas; the
+ * transposed convolution additionally by the adjoint identity with the (pinned) direct
+ * convolution and by closed forms on tiny inputs.
  */
 #include <math.h>
 #include <stdint.h>
@@ -290,6 +299,177 @@ int oracle_fused_conv(const oracle_attrs* a, const double* x, const double* w, c
           if (abssum) abssum[yi] = aacc;
         }
   }
+  return OR_OK;
+}
+
+/* ------------------------------------------------------------ transposed convolution */
+
+typedef struct {
+  int rank;                    /* rank of X and W: 3, 4 or 5 */
+  int64_t x_shape[5];          /* (N, C, spatial...) */
+  int64_t w_shape[5];          /* (C, M / group, kernel...) */
+  int64_t group;
+  int n_strides, n_dilations, n_pads, n_output_padding;  /* 0 = attribute absent */
+  int64_t strides[3], dilations[3], pads[6], output_padding[3];
+  int activation;
+  int n_act_params;            /* -1 = attribute absent */
+  double act_params[2];
+} oracle_tattrs;
+
+/* Resolve a transposed convolution: per axis
+ *   out = (in - 1) * stride - pad_begin - pad_end + dilation * (k - 1) + output_padding + 1
+ * with stride, dilation >= 1, pads >= 0 and 0 <= output_padding < stride; C = W.dim0,
+ * group divides C, M = W.dim1 * group. The activation rules are those of the direct
+ * convolution. */
+int oracle_resolve_transpose(const oracle_tattrs* a, oracle_geom* g) {
+  if (!a || !g) return OR_NULL;
+  memset(g, 0, sizeof(*g));
+  if (a->rank < 3 || a->rank > 5) return OR_BAD_RANK;
+  const int sr = a->rank - 2;
+  g->spatial_rank = sr;
+  if (a->n_strides && a->n_strides != sr) return OR_ATTR_LENGTH;
+  if (a->n_dilations && a->n_dilations != sr) return OR_ATTR_LENGTH;
+  if (a->n_pads && a->n_pads != 2 * sr) return OR_ATTR_LENGTH;
+  if (a->n_output_padding && a->n_output_padding != sr) return OR_ATTR_LENGTH;
+  for (int j = 0; j < 3; ++j) {
+    const int ax = j - (3 - sr);
+    int64_t op = 0;
+    if (ax < 0) {
+      g->in[j] = 1; g->k[j] = 1; g->s[j] = 1; g->d[j] = 1;
+    } else {
+      g->in[j] = a->x_shape[2 + ax];
+      g->k[j] = a->w_shape[2 + ax];
+      g->s[j] = a->n_strides ? a->strides[ax] : 1;
+      g->d[j] = a->n_dilations ? a->dilations[ax] : 1;
+      g->pad_begin[j] = a->n_pads ? a->pads[ax] : 0;
+      g->pad_end[j] = a->n_pads ? a->pads[sr + ax] : 0;
+      op = a->n_output_padding ? a->output_padding[ax] : 0;
+    }
+    if (g->k[j] < 1 || g->s[j] < 1 || g->d[j] < 1) return OR_ATTR_VALUE;
+    if (g->pad_begin[j] < 0 || g->pad_end[j] < 0) return OR_ATTR_VALUE;
+    if (op < 0 || op >= g->s[j]) return OR_ATTR_VALUE;
+    g->out[j] = (g->in[j] - 1) * g->s[j] - g->pad_begin[j] - g->pad_end[j] +
+                g->d[j] * (g->k[j] - 1) + op + 1;
+    if (g->out[j] < 1) return OR_EMPTY_OUTPUT;
+  }
+  g->N = a->x_shape[0];
+  g->C = a->x_shape[1];
+  g->G = a->group;
+  if (g->G < 1 || a->w_shape[0] != g->C || g->C % g->G != 0) return OR_GROUP;
+  g->Cg = g->C / g->G;
+  g->Mg = a->w_shape[1];
+  g->M = g->Mg * g->G;
+  if (g->N < 1 || g->C < 1 || g->Mg < 1) return OR_BAD_RANK;
+  /* the activation and its parameters, as for the direct convolution */
+  oracle_attrs t;
+  memset(&t, 0, sizeof(t));
+  t.activation = a->activation;
+  t.n_act_params = a->n_act_params;
+  t.act_params[0] = a->act_params[0];
+  t.act_params[1] = a->act_params[1];
+  const int act = t.activation, np = t.n_act_params;
+  if (act < 0 || act >= A_COUNT) return OR_ACTIVATION;
+  if (act == A_LEAKYRELU && np != 1) return OR_ACT_PARAMS;
+  if ((act == A_HARDSIGMOID || act == A_CLIP) && np != 2) return OR_ACT_PARAMS;
+  if ((act == A_QUICKGELU || act == A_ELU || act == A_THRESHOLDEDRELU || act == A_GELU) && np > 1)
+    return OR_ACT_PARAMS;
+  double alpha = 0.0, beta = 0.0;
+  if (act == A_HARDSIGMOID) { alpha = 0.2; beta = 0.5; }
+  else if (act == A_LEAKYRELU) alpha = 0.01;
+  else if (act == A_QUICKGELU) alpha = 1.702;
+  else if (act == A_ELU || act == A_THRESHOLDEDRELU) alpha = 1.0;
+  if (np >= 1) alpha = t.act_params[0];
+  if (np >= 2) beta = t.act_params[1];
+  g->alpha = alpha;
+  g->beta = beta;
+  return OR_OK;
+}
+
+int oracle_transpose_output_shape(const oracle_tattrs* a, int64_t* y_shape) {
+  oracle_geom g;
+  const int st = oracle_resolve_transpose(a, &g);
+  if (st != OR_OK) return st;
+  y_shape[0] = g.N;
+  y_shape[1] = g.M;
+  for (int i = 0; i < g.spatial_rank; ++i) y_shape[2 + i] = g.out[3 - g.spatial_rank + i];
+  return OR_OK;
+}
+
+/*
+ * Scatter form: for every n, input channel c (group grp = c / Cg), output channel
+ * m = grp*Mg + mm, input position i and tap t,
+ *   s[n, m, i*stride - pad_begin + t*dilation] += x[n, c, i] * w[c, mm, t]
+ * when that output position exists; then y = act(s + b[m] + z). abssum accumulates
+ * |x * w| over the same terms. (n, group) pairs write disjoint outputs, so they run in
+ * parallel.
+ */
+int oracle_conv_transpose(const oracle_tattrs* a, const double* x, const double* w,
+                          const double* b, const double* z, double* y, double* abssum,
+                          int nthreads) {
+  oracle_geom g;
+  const int st = oracle_resolve_transpose(a, &g);
+  if (st != OR_OK) return st;
+  if (!x || !w || !y) return OR_NULL;
+  const int64_t ID = g.in[0], IH = g.in[1], IW = g.in[2];
+  const int64_t KD = g.k[0], KH = g.k[1], KW = g.k[2];
+  const int64_t OD = g.out[0], OH = g.out[1], OW = g.out[2];
+  const int64_t P = OD * OH * OW, IS = ID * IH * IW, KS = KD * KH * KW;
+  double* acc = (double*)calloc((size_t)(g.N * g.M * P), sizeof(double));
+  double* aacc = (double*)calloc((size_t)(g.N * g.M * P), sizeof(double));
+  if (!acc || !aacc) {
+    free(acc);
+    free(aacc);
+    return OR_NULL;
+  }
+  const int64_t NG = g.N * g.G;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (int64_t ng = 0; ng < NG; ++ng) {
+    const int64_t n = ng / g.G, grp = ng % g.G;
+    for (int64_t cc = 0; cc < g.Cg; ++cc) {
+      const int64_t c = grp * g.Cg + cc;
+      const double* xp = x + (n * g.C + c) * IS;
+      for (int64_t mm = 0; mm < g.Mg; ++mm) {
+        const int64_t m = grp * g.Mg + mm;
+        const double* wp = w + (c * g.Mg + mm) * KS;
+        double* sp = acc + (n * g.M + m) * P;
+        double* ap = aacc + (n * g.M + m) * P;
+        for (int64_t iz = 0; iz < ID; ++iz)
+          for (int64_t iy = 0; iy < IH; ++iy)
+            for (int64_t ix = 0; ix < IW; ++ix) {
+              const double xv = xp[(iz * IH + iy) * IW + ix];
+              for (int64_t kz = 0; kz < KD; ++kz) {
+                const int64_t oz = iz * g.s[0] - g.pad_begin[0] + kz * g.d[0];
+                if (oz < 0 || oz >= OD) continue;
+                for (int64_t ky = 0; ky < KH; ++ky) {
+                  const int64_t oy = iy * g.s[1] - g.pad_begin[1] + ky * g.d[1];
+                  if (oy < 0 || oy >= OH) continue;
+                  for (int64_t kx = 0; kx < KW; ++kx) {
+                    const int64_t ox = ix * g.s[2] - g.pad_begin[2] + kx * g.d[2];
+                    if (ox < 0 || ox >= OW) continue;
+                    const double p = xv * wp[(kz * KH + ky) * KW + kx];
+                    const int64_t o = (oz * OH + oy) * OW + ox;
+                    sp[o] += p;
+                    ap[o] += fabs(p);
+                  }
+                }
+              }
+            }
+      }
+    }
+  }
+  for (int64_t i = 0; i < g.N * g.M * P; ++i) {
+    const int64_t m = (i / P) % g.M;
+    double v = acc[i];
+    if (b) v += b[m];
+    if (z) v += z[i];
+    y[i] = oracle_activation(a->activation, v, g.alpha, g.beta);
+    if (abssum) abssum[i] = aacc[i];
+  }
+  free(acc);
+  free(aacc);
   return OR_OK;
 }
 
