@@ -13,7 +13,8 @@ from typing import Optional, Sequence
 from . import _lib
 from ._lib import ROUTES, ROUTE_NAMES, STATUS
 
-__all__ = ["FconvError", "FusedConvPlan", "fused_conv", "plan_for", "load_library", "build"]
+__all__ = ["FconvError", "FusedConvPlan", "fused_conv", "conv_transpose", "plan_for", "load_library",
+           "build"]
 
 
 class FconvError(RuntimeError):
@@ -55,7 +56,8 @@ class FusedConvPlan:
                  dilations=None, pads=None, auto_pad: str = "NOTSET", kernel_shape=None,
                  activation: Optional[str] = None, activation_params=None, device: int = -1,
                  route: str = "auto", split_k: int = 0, tile_n: int = 0, z_shape=None,
-                 a_path: str = "auto", max_ctas: int = 0):
+                 a_path: str = "auto", max_ctas: int = 0, transposed: bool = False,
+                 output_padding=None):
         lib = _lib.load()
         self._lib = lib
         self._ptr = ctypes.c_void_p()
@@ -64,13 +66,19 @@ class FusedConvPlan:
         self.w_shape = tuple(int(v) for v in w_shape)
         self.has_bias = bool(has_bias)
         self.has_z = bool(has_z)
+        # B has M entries: W.dim0 for the direct form, W.dim1 * group for the transposed one
+        if transposed:
+            bias_len = int(w_shape[1]) * int(group) if len(w_shape) > 1 else 0
+        else:
+            bias_len = int(w_shape[0]) if len(w_shape) else 0
         # Z must match Y; when the caller does not give Z's shape, derive Y's first.
         if has_z and z_shape is None:
             probe = _lib.make_desc(dtype, x_shape, w_shape, has_bias=has_bias,
-                                   bias_len=w_shape[0] if len(w_shape) else 0, group=group,
+                                   bias_len=bias_len, group=group,
                                    strides=strides, dilations=dilations, pads=pads,
                                    auto_pad=auto_pad, kernel_shape=kernel_shape,
-                                   activation=activation, activation_params=activation_params)
+                                   activation=activation, activation_params=activation_params,
+                                   transposed=transposed, output_padding=output_padding)
             tmp = ctypes.c_void_p()
             _check(lib.fconv_plan_create(ctypes.byref(probe), device, ctypes.byref(tmp)),
                    "fconv_plan_create")
@@ -80,11 +88,12 @@ class FusedConvPlan:
             lib.fconv_destroy(tmp)
             z_shape = tuple(ys[i] for i in range(rk.value))
         desc = _lib.make_desc(dtype, x_shape, w_shape, has_bias=has_bias,
-                              bias_len=w_shape[0] if len(w_shape) else 0,
+                              bias_len=bias_len,
                               z_shape=z_shape if has_z else None, group=group, strides=strides,
                               dilations=dilations, pads=pads, auto_pad=auto_pad,
                               kernel_shape=kernel_shape, activation=activation,
-                              activation_params=activation_params)
+                              activation_params=activation_params, transposed=transposed,
+                              output_padding=output_padding)
         opts = _lib.FconvOptions(ROUTES[route], int(split_k), int(tile_n),
                                  {"auto": 0, "gather": 1, "tma": 2}[a_path], int(max_ctas))
         _check(lib.fconv_plan_create_ex(ctypes.byref(desc), device, ctypes.byref(opts),
@@ -160,7 +169,8 @@ def plan_for(x, w, b=None, z=None, **attrs) -> FusedConvPlan:
                         for k, v in attrs.items())))
     p = _plans.get(key)
     if p is None:
-        if b is not None and (b.dim() != 1 or b.shape[0] != w.shape[0]):
+        m = w.shape[1] * attrs.get("group", 1) if attrs.get("transposed") else w.shape[0]
+        if b is not None and (b.dim() != 1 or b.shape[0] != m):
             raise FconvError(8, "bias")
         p = FusedConvPlan(dtype, x.shape, w.shape, has_bias=b is not None,
                           has_z=z is not None,
@@ -183,4 +193,17 @@ def fused_conv(x, w, b=None, z=None, *, group: int = 1, strides=None, dilations=
                  auto_pad=auto_pad, kernel_shape=kernel_shape, activation=activation,
                  activation_params=activation_params, route=route, split_k=split_k,
                  tile_n=tile_n, a_path=a_path, max_ctas=max_ctas)
+    return p.run(x, w, b, z, y=out)
+
+
+def conv_transpose(x, w, b=None, z=None, *, group: int = 1, strides=None, dilations=None,
+                   pads=None, output_padding=None, activation: Optional[str] = None,
+                   activation_params=None, out=None):
+    """Y = act(convT(X, W) + B + Z) on CUDA tensors: the transposed convolution in gather
+    form, W of shape (C, M/group, kernel...)."""
+    if not x.is_cuda:
+        raise ValueError("conv_transpose runs on CUDA tensors only")
+    p = plan_for(x, w, b, z, group=group, strides=strides, dilations=dilations, pads=pads,
+                 activation=activation, activation_params=activation_params, transposed=True,
+                 output_padding=output_padding)
     return p.run(x, w, b, z, y=out)

@@ -12,7 +12,8 @@ AUTO_PAD = {"NOTSET": 0, "SAME_UPPER": 1, "SAME_LOWER": 2, "VALID": 3}
 ACTIVATIONS = {None: 0, "Relu": 1, "LeakyRelu": 2, "Sigmoid": 3, "Tanh": 4, "HardSigmoid": 5,
                "HardSwish": 6, "Clip": 7, "QuickGelu": 8, "Elu": 9, "Gelu": 10, "FastGelu": 11,
                "Softplus": 12, "ThresholdedRelu": 13, "Erf": 14}
-ROUTES = {"auto": 0, "direct": 1, "igemm_tc": 2, "depthwise": 3, "grouped": 4}
+ROUTES = {"auto": 0, "direct": 1, "igemm_tc": 2, "depthwise": 3, "grouped": 4,
+          "transposed": 5}
 ROUTE_NAMES = {v: k for k, v in ROUTES.items()}
 STATUS = {0: "OK", 1: "E_NULL", 2: "E_RANK", 3: "E_ATTR_LENGTH", 4: "E_ATTR_VALUE",
           5: "E_PADS_WITH_AUTOPAD", 6: "E_KERNEL_SHAPE", 7: "E_GROUP", 8: "E_BIAS_SHAPE",
@@ -34,7 +35,9 @@ class FconvDesc(ctypes.Structure):
                 ("kernel_shape", I64 * 3), ("strides", I64 * 3), ("dilations", I64 * 3),
                 ("pads", I64 * 6),
                 ("activation", ctypes.c_int), ("n_act_params", ctypes.c_int),
-                ("act_params", ctypes.c_float * 2)]
+                ("act_params", ctypes.c_float * 2),
+                ("transposed", ctypes.c_int), ("n_output_padding", ctypes.c_int),
+                ("output_padding", I64 * 3)]
 
 
 class FconvOptions(ctypes.Structure):
@@ -86,7 +89,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
 def make_desc(dtype: int, x_shape, w_shape, *, has_bias: bool = False, bias_len: int = 0,
               z_shape=None, group: int = 1, strides=None, dilations=None, pads=None,
               auto_pad: str = "NOTSET", kernel_shape=None, activation=None,
-              activation_params=None) -> FconvDesc:
+              activation_params=None, transposed: bool = False,
+              output_padding=None) -> FconvDesc:
     d = FconvDesc()
     d.dtype = dtype
     d.rank = len(x_shape) if len(x_shape) == len(w_shape) else -1
@@ -118,6 +122,8 @@ def make_desc(dtype: int, x_shape, w_shape, *, has_bias: bool = False, bias_len:
     d.n_strides = put(d.strides, strides, 3)
     d.n_dilations = put(d.dilations, dilations, 3)
     d.n_pads = put(d.pads, pads, 6)
+    d.transposed = 1 if transposed else 0
+    d.n_output_padding = put(d.output_padding, output_padding, 3)
     if activation not in ACTIVATIONS:
         raise ValueError(f"unknown activation {activation!r}")
     d.activation = ACTIVATIONS[activation]

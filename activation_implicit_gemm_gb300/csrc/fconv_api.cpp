@@ -31,6 +31,7 @@ struct fconv_plan {
   IgemmConfig igemm;
   size_t workspace;
   int sms;
+  double flops;   // algorithmic FLOPs of one run
 };
 
 namespace {
@@ -71,16 +72,19 @@ fconv_status resolve(const fconv_desc* d, fconv_plan* p) {
   for (int i = 0; i < r; ++i)
     if (d->x_shape[i] < 1 || d->w_shape[i] < 1) return FCONV_E_RANK;
   if ((d->n_kernel_shape && d->n_kernel_shape != sr) || (d->n_strides && d->n_strides != sr) ||
-      (d->n_dilations && d->n_dilations != sr) || (d->n_pads && d->n_pads != 2 * sr))
+      (d->n_dilations && d->n_dilations != sr) || (d->n_pads && d->n_pads != 2 * sr) ||
+      (d->n_output_padding && d->n_output_padding != sr))
     return FCONV_E_ATTR_LENGTH;
-  int64_t in[3], k[3], s[3], dl[3], pb[3], pe[3], out[3];
+  const bool tr = d->transposed != 0;
+  int64_t in[3], k[3], s[3], dl[3], pb[3], pe[3], out[3], op[3];
   for (int j = 0; j < 3; ++j) {
     const int ax = j - (3 - sr);
     if (ax < 0) {
       in[j] = k[j] = s[j] = dl[j] = 1;
-      pb[j] = pe[j] = 0;
+      pb[j] = pe[j] = op[j] = 0;
       continue;
     }
+    op[j] = d->n_output_padding ? d->output_padding[ax] : 0;
     in[j] = d->x_shape[2 + ax];
     k[j] = d->w_shape[2 + ax];
     s[j] = d->n_strides ? d->strides[ax] : 1;
@@ -93,7 +97,17 @@ fconv_status resolve(const fconv_desc* d, fconv_plan* p) {
     if (s[j] < 1 || dl[j] < 1 || pb[j] < 0 || pe[j] < 0 || k[j] < 1) return FCONV_E_ATTR_VALUE;
   if (d->auto_pad < FCONV_PAD_NOTSET || d->auto_pad > FCONV_PAD_VALID) return FCONV_E_ATTR_VALUE;
   if (d->auto_pad != FCONV_PAD_NOTSET && d->n_pads) return FCONV_E_PADS_WITH_AUTOPAD;
-  for (int j = 0; j < 3; ++j) {
+  // output_padding: below the stride on the transposed form, zero on the direct one
+  for (int j = 0; j < 3; ++j)
+    if (op[j] < 0 || (tr ? op[j] >= s[j] : op[j] != 0)) return FCONV_E_ATTR_VALUE;
+  if (tr && (d->auto_pad == FCONV_PAD_SAME_UPPER || d->auto_pad == FCONV_PAD_SAME_LOWER))
+    return FCONV_E_UNSUPPORTED;
+  for (int j = 0; j < 3 && tr; ++j) {
+    if (d->auto_pad == FCONV_PAD_VALID) pb[j] = pe[j] = 0;
+    out[j] = (in[j] - 1) * s[j] - pb[j] - pe[j] + dl[j] * (k[j] - 1) + op[j] + 1;
+    if (out[j] < 1) return FCONV_E_OUTPUT_EMPTY;
+  }
+  for (int j = 0; j < 3 && !tr; ++j) {
     const int64_t ext = (k[j] - 1) * dl[j] + 1;
     if (d->auto_pad == FCONV_PAD_SAME_UPPER || d->auto_pad == FCONV_PAD_SAME_LOWER) {
       out[j] = (in[j] + s[j] - 1) / s[j];
@@ -108,8 +122,13 @@ fconv_status resolve(const fconv_desc* d, fconv_plan* p) {
     }
     if (out[j] < 1) return FCONV_E_OUTPUT_EMPTY;
   }
-  const int64_t N = d->x_shape[0], C = d->x_shape[1], M = d->w_shape[0], G = d->group;
-  if (G < 1 || M % G != 0 || d->w_shape[1] * G != C) return FCONV_E_GROUP;
+  const int64_t N = d->x_shape[0], C = d->x_shape[1], G = d->group;
+  const int64_t M = tr ? d->w_shape[1] * G : d->w_shape[0];
+  if (tr) {
+    if (G < 1 || d->w_shape[0] != C || C % G != 0) return FCONV_E_GROUP;
+  } else if (G < 1 || M % G != 0 || d->w_shape[1] * G != C) {
+    return FCONV_E_GROUP;
+  }
   if (d->has_bias && d->bias_len != M) return FCONV_E_BIAS_SHAPE;
 
   const int act = (int)d->activation, np = d->n_act_params;
@@ -158,6 +177,25 @@ fconv_status resolve(const fconv_desc* d, fconv_plan* p) {
   g.dD = (int)dl[0]; g.dH = (int)dl[1]; g.dW = (int)dl[2];
   g.pD = (int)pb[0]; g.pH = (int)pb[1]; g.pW = (int)pb[2];
   g.act = act; g.alpha = alpha; g.beta = beta;
+  g.transposed = tr ? 1 : 0;
+  // FLOPs: 2 * N * M * P * Kg for the direct form (every tap of every output); for the
+  // transposed form 2 * N * C * M/group * the (input position, tap) pairs that land on an
+  // output, counted per axis
+  if (tr) {
+    double pairs = 1.0;
+    for (int j = 0; j < 3; ++j) {
+      int64_t cnt = 0;
+      for (int64_t i = 0; i < in[j]; ++i)
+        for (int64_t t = 0; t < k[j]; ++t) {
+          const int64_t o = i * s[j] - pb[j] + t * dl[j];
+          if (o >= 0 && o < out[j]) ++cnt;
+        }
+      pairs *= (double)cnt;
+    }
+    p->flops = 2.0 * (double)N * (double)C * (double)(M / G) * pairs;
+  } else {
+    p->flops = 2.0 * (double)N * (double)M * (double)(out[0] * out[1] * out[2]) * (double)Kg;
+  }
   g.has_bias = d->has_bias ? 1 : 0;
   g.has_z = d->has_z ? 1 : 0;
   g.P = (long long)(out[0] * out[1] * out[2]);
@@ -229,7 +267,13 @@ fconv_status create(const fconv_desc* d, int device, const fconv_options* o, fco
   // which were faster on the 3-D grouped conv X[2,32,16,64,64] W[64,8,3,3,3] group 4
   // (C/group * kernel = 216).
   const bool small_groups = p->g.G > 1 && p->g.Cg <= 16 && p->g.Mg <= 32 && p->g.Kg <= 64;
-  if (want == FCONV_ROUTE_AUTO) {
+  if (p->g.transposed) {
+    // the transposed form has one route
+    if ((want != FCONV_ROUTE_AUTO && want != FCONV_ROUTE_TRANSPOSED) ||
+        !transposed_supported(p->g))
+      st = FCONV_E_UNSUPPORTED;
+    route = FCONV_ROUTE_TRANSPOSED;
+  } else if (want == FCONV_ROUTE_AUTO) {
     if (depthwise_supported(p->g)) route = FCONV_ROUTE_DEPTHWISE;
     else if (small_groups && grouped_supported(p->g)) route = FCONV_ROUTE_GROUPED;
     else if (igemm_tc_supported(p->g, tile_n)) route = FCONV_ROUTE_IGEMM_TC;
@@ -242,6 +286,7 @@ fconv_status create(const fconv_desc* d, int device, const fconv_options* o, fco
     st = FCONV_E_UNSUPPORTED;
   } else if (want != FCONV_ROUTE_DIRECT && want != FCONV_ROUTE_DEPTHWISE &&
              want != FCONV_ROUTE_IGEMM_TC && want != FCONV_ROUTE_GROUPED) {
+    // includes FCONV_ROUTE_TRANSPOSED for a direct convolution
     st = FCONV_E_UNSUPPORTED;
   }
   if (st == FCONV_OK && route == FCONV_ROUTE_IGEMM_TC && o && o->tile_n &&
@@ -322,7 +367,8 @@ fconv_status fconv_plan_work(const fconv_plan* p, double* flops, double* bytes) 
   const ConvGeom& g = p->g;
   const double es = g.dtype == FCONV_F16 ? 2.0 : 4.0;
   const double ny = (double)g.N * g.M * (double)g.P;
-  if (flops) *flops = 2.0 * ny * (double)g.Kg;
+  (void)ny;
+  if (flops) *flops = p->flops;
   if (bytes) {
     double b = (double)g.N * g.C * (double)g.IS + (double)g.M * g.Kg + ny;
     if (g.has_bias) b += g.M;
@@ -352,6 +398,7 @@ fconv_status fconv_run(const fconv_plan* p, const void* x, const void* w, const 
     case FCONV_ROUTE_DIRECT: err = launch_direct(p->g, a, stream); break;
     case FCONV_ROUTE_DEPTHWISE: err = launch_depthwise(p->g, a, stream); break;
     case FCONV_ROUTE_GROUPED: err = launch_grouped(p->g, a, stream); break;
+    case FCONV_ROUTE_TRANSPOSED: err = launch_transposed(p->g, a, stream); break;
     case FCONV_ROUTE_IGEMM_TC: err = launch_igemm_tc(p->g, p->igemm, a, stream); break;
     default: return FCONV_E_UNSUPPORTED;
   }

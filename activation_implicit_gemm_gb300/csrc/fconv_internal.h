@@ -32,6 +32,7 @@ struct ConvGeom {
   int KV;                       // KD*KH*KW
   int Kg;                       // Cg*KV
   int max_ctas;                 // cap on persistent CTAs (0 = none)
+  int transposed;               // transposed convolution (W is (C, M/group, kernel...))
 };
 
 struct ConvArgs {
@@ -61,6 +62,8 @@ int read_and_clear_dw_error(void* stream, unsigned* value);
 int launch_grouped(const ConvGeom& g, const ConvArgs& a, void* stream);
 bool grouped_supported(const ConvGeom& g);
 int read_and_clear_grouped_error(void* stream, unsigned* value);
+int launch_transposed(const ConvGeom& g, const ConvArgs& a, void* stream);
+bool transposed_supported(const ConvGeom& g);
 
 // tcgen05 implicit GEMM: dispatch between the two A paths (k_igemm_tc.cu).
 int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, void* stream);

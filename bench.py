@@ -41,8 +41,9 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # CUDA-core f32 FMA peak of a GB300: 152 SMs x 128 FMA lanes x 2 FLOP per FMA x the
-# maximum SM clock (2070 MHz) = 80.5 TFLOP/s. The depthwise, grouped and direct routes
-# compute on these lanes, so their compute roofline is this one, not the tensor cores'.
+# maximum SM clock (2070 MHz) = 80.5 TFLOP/s. The depthwise, grouped, direct and transposed
+# routes compute on these lanes, so their compute roofline is this one, not the tensor
+# cores'.
 SMS, FMA_LANES_PER_SM, SM_MAX_MHZ = 152, 128, 2070.0
 
 
@@ -153,7 +154,7 @@ def oracle_tensors(case):
     return workloads.make_inputs(case, ys), ys
 
 
-CUDA_CORE_ROUTES = ("depthwise", "grouped", "direct")
+CUDA_CORE_ROUTES = ("depthwise", "grouped", "direct", "transposed")
 
 
 def bound_of(flops, bytes_, peaks, route="igemm_tc"):
@@ -177,6 +178,45 @@ def main_kernel_name(case, route):
         return "igemm_tma_kernel" if case.w_shape[1] % 64 == 0 else "igemm_patch_kernel"
     return {"depthwise": "dw_tile_kernel", "direct": "direct_conv_kernel",
             "grouped": "grouped_kernel"}[route]
+
+
+def measure_next_rows(dev, stream, flush, peaks):
+    """Rows beyond the suite, timed after it and outside its value: each workload of
+    workloads.TRANSPOSED_CASES through the library's transposed route, L2 flushed before
+    every run, CUDA events on the launching stream."""
+    import torch
+    import activation_implicit_gemm_gb300 as fc
+    from activation_implicit_gemm_gb300 import _lib
+    rows = []
+    for case in workloads.TRANSPOSED_CASES:
+        dt = _lib.F16 if case["dtype"] == "f16" else _lib.F32
+        plan = fc.FusedConvPlan(dt, case["x_shape"], case["w_shape"], has_bias=True,
+                                has_z=True, transposed=True, **case["attrs"])
+        t = workloads.make_transposed_inputs(case, plan.y_shape)
+        d = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in t.items()}
+        y = torch.empty(plan.y_shape, dtype=d["x"].dtype, device=dev)
+        reps = 10
+        for _ in range(3):
+            plan.run(d["x"], d["w"], d["b"], d["z"], y=y, stream=stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            plan.run(d["x"], d["w"], d["b"], d["z"], y=y, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in ev) / reps
+        tf = plan.flops / (ms * 1e-3) / 1e12
+        bnd = bound_of(plan.flops, plan.bytes, peaks, plan.route)
+        frac = (tf / compute_peak(bnd, peaks) if bnd in ("tensor", "alu")
+                else plan.bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"])
+        rows.append({"row": "NEXT-4 transposed convolution (gather form)", "conv": case["name"],
+                     "route": plan.route, "us": round(ms * 1e3, 2), "tflops": round(tf, 2),
+                     "gbs": round(plan.bytes / (ms * 1e-3) / 1e9, 1), "bound": bnd,
+                     "frac_of_bound": round(frac, 4), "flops": plan.flops,
+                     "bytes": plan.bytes, "kernel": "convt_kernel"})
+    return rows
 
 
 def run_ours(args):
@@ -362,6 +402,8 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     e2e_value = job_tflops(total_flops, ws_n, e2e_steps, e2e_ms)
 
+    next_rows = [] if args.conv else measure_next_rows(dev, stream, flush, peaks)
+
     out = {"metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws_n,
            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
@@ -385,6 +427,8 @@ def run_ours(args):
                    "overlap": "conv i+1's inputs upload and conv i-1's output downloads "
                               "while conv i runs (copy streams ordered by events)"},
            "gpu_launches": launches_per_step * K, "clocks": clocks}
+    if next_rows:
+        out["next_rows"] = next_rows
     if args.conv:
         out["config"]["workload"] = "subset: " + args.conv
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline and not args.conv:

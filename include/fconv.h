@@ -105,10 +105,13 @@ typedef enum {
   FCONV_ROUTE_IGEMM_TC = 2, /* tcgen05 implicit GEMM (float16): in-kernel im2col gather to
                                shared memory, accumulator in tensor memory, fused epilogue */
   FCONV_ROUTE_DEPTHWISE = 3, /* CUDA-core depthwise 2-D kernel (C == M == group) */
-  FCONV_ROUTE_GROUPED = 4    /* CUDA-core grouped conv with small groups (C/group <= 16,
+  FCONV_ROUTE_GROUPED = 4,   /* CUDA-core grouped conv with small groups (C/group <= 16,
                                 M/group <= 32), any rank: shared-memory halo box per (image,
                                 group, output box), f32 accumulation. The planner picks it
                                 when also C/group * prod(kernel) <= 64. */
+  FCONV_ROUTE_TRANSPOSED = 5 /* CUDA-core transposed conv in gather form (desc.transposed):
+                                a warp takes 32 outputs of one stride phase, so its lanes
+                                share the valid taps; any rank and group, f32 accumulation */
 } fconv_route;
 
 /* Operator inputs and attributes (manifest "inputs", "attributes"; README "Attributes").
@@ -133,6 +136,17 @@ typedef struct {
   fconv_act activation;
   int n_act_params;             /* -1: attribute absent; else 0..2 values given */
   float act_params[2];
+  /* Transposed convolution (ExecuTorch WebGPU PR #20849, the transposed form of
+   * aten.convolution.default): Y = act(convT(X, W) + B + Z) where input position i adds
+   * X[n, c, i] * W[c, m, k] to output position i*stride - pad_begin + k*dilation. W is then
+   * (C, M/group, kernel...), M = W.dim1 * group, and per axis
+   *   out = (in - 1)*stride - pad_begin - pad_end + dilation*(k - 1) + output_padding + 1
+   * with 0 <= output_padding < stride. auto_pad must be NOTSET or VALID. With transposed = 0
+   * output_padding must be absent or all zero. Zero-initialised descriptors are direct
+   * convolutions. */
+  int transposed;
+  int n_output_padding;         /* 0 = absent; else spatialRank values */
+  int64_t output_padding[3];
 } fconv_desc;
 
 /* Planner overrides, for tests and experiments. Zero-initialise for defaults. */

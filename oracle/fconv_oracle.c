@@ -350,8 +350,10 @@ int oracle_resolve_transpose(const oracle_tattrs* a, oracle_geom* g) {
     if (op < 0 || op >= g->s[j]) return OR_ATTR_VALUE;
     g->out[j] = (g->in[j] - 1) * g->s[j] - g->pad_begin[j] - g->pad_end[j] +
                 g->d[j] * (g->k[j] - 1) + op + 1;
-    if (g->out[j] < 1) return OR_EMPTY_OUTPUT;
   }
+  /* every attribute value is checked before any output extent, as for the direct form */
+  for (int j = 0; j < 3; ++j)
+    if (g->out[j] < 1) return OR_EMPTY_OUTPUT;
   g->N = a->x_shape[0];
   g->C = a->x_shape[1];
   g->G = a->group;

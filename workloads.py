@@ -186,3 +186,24 @@ def case_by_name(name: str) -> ConvCase:
         if c.name == name:
             return c
     raise KeyError(name)
+
+
+# Widening beyond the benchmark suite (measured next to it, not part of its value): the
+# transposed convolution of an upsampling stage, W of shape (C, M/group, k, k).
+TRANSPOSED_CASES = [
+    dict(name="convT_up_256to128_k4_s2", dtype="f16", x_shape=(8, 256, 32, 32),
+         w_shape=(256, 128, 4, 4), attrs=dict(strides=[2, 2], pads=[1, 1, 1, 1],
+                                              activation="Relu"), seed=0xF1C0),
+]
+
+
+def make_transposed_inputs(case: dict, y_shape: Sequence[int]) -> dict:
+    """X ~ N(0,1), W ~ N(0,1)/sqrt(C/group * k*k), B, Z ~ N(0,1) for a transposed case."""
+    xs, ws = case["x_shape"], case["w_shape"]
+    g = case["attrs"].get("group", 1)
+    kg = (ws[0] // g) * int(np.prod(ws[2:]))
+    s, dt = case["seed"], case["dtype"]
+    return {"x": draw(s, xs, "normal", 1.0, dt),
+            "w": draw(s + 1, ws, "normal", 1.0 / float(np.sqrt(kg)), dt),
+            "b": draw(s + 2, (y_shape[1],), "normal", 1.0, dt),
+            "z": draw(s + 3, y_shape, "normal", 1.0, dt)}
