@@ -18,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfconv.so")
 
 SOURCES = ["fconv_api.cpp", "k_direct.cu", "k_depthwise.cu", "k_grouped.cu", "k_igemm_tc.cu",
-           "k_igemm_patch.cu", "k_transposed.cu", "fconv_noalloc.cu"]
+           "k_igemm_patch.cu", "k_igemm_tf32.cu", "k_transposed.cu", "fconv_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -87,6 +87,14 @@ int igemm_patch_launches(const ConvGeom& g, const IgemmConfig& c);
 int launch_igemm_patch(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, void* stream);
 int read_and_clear_patch_error(void* stream, unsigned* value);
 
+// The fp32 3xTF32 kernel (k_igemm_tf32.cu): C/group a multiple of 32.
+bool igemm_tf32_capable(const ConvGeom& g, int max_px);
+long long igemm_tf32_mtiles(const ConvGeom& g, int max_px);
+int igemm_tf32_chunks(const ConvGeom& g);
+size_t igemm_tf32_workspace_bytes(const ConvGeom& g, const IgemmConfig& c);
+int launch_igemm_tf32(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, void* stream);
+int read_and_clear_tf32_error(void* stream, unsigned* value);
+
 // cuTensorMapEncodeTiled from the driver (null when unavailable).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,

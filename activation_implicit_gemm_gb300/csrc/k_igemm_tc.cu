@@ -595,10 +595,13 @@ int launch_splitk_reduce(const ConvGeom& g, int splits, const float* part, const
 bool igemm_tc_tma_capable(const ConvGeom& g) { return tma_shape(g).ok; }
 
 bool igemm_tc_supported(const ConvGeom& g, int max_px) {
+  if (g.dtype == FCONV_F32) return igemm_tf32_capable(g, max_px);
   return tma_shape(g, max_px).ok || igemm_patch_capable(g, max_px);
 }
 
 int igemm_tc_resolve_path(const ConvGeom& g, int max_px, int requested) {
+  // fp32: the 3xTF32 kernel, fed by TMA boxes of the repacked copies
+  if (g.dtype == FCONV_F32) return (requested != 1 && igemm_tf32_capable(g, max_px)) ? 2 : 0;
   if (requested == 2) return tma_shape(g, max_px).ok ? 2 : 0;
   if (requested == 1) return igemm_patch_capable(g, max_px) ? 1 : 0;
   if (tma_shape(g, max_px).ok) return 2;
@@ -606,6 +609,7 @@ int igemm_tc_resolve_path(const ConvGeom& g, int max_px, int requested) {
 }
 
 size_t igemm_tc_workspace_bytes(const ConvGeom& g, const IgemmConfig& c) {
+  if (g.dtype == FCONV_F32) return igemm_tf32_workspace_bytes(g, c);
   if (c.a_path == 1) return igemm_patch_workspace_bytes(g, c);
   size_t b = tma_prep_bytes(g) + tma_pack_bytes(g);
   if (c.split_k > 1) b += (size_t)c.split_k * (size_t)g.N * (size_t)g.M * (size_t)g.P * 4;
@@ -613,27 +617,31 @@ size_t igemm_tc_workspace_bytes(const ConvGeom& g, const IgemmConfig& c) {
 }
 
 int igemm_tc_launches(const ConvGeom& g, const IgemmConfig& c) {
+  if (g.dtype == FCONV_F32) return 3;  // prologue, 3xTF32 GEMM, reduce + epilogue
   if (c.a_path == 1) return igemm_patch_launches(g, c);
   return 2 + (c.split_k > 1 ? 1 : 0);  // prologue, main kernel, split-K reduce
 }
 
 long long igemm_tc_mtiles(const ConvGeom& g, int a_path, int max_px) {
+  if (g.dtype == FCONV_F32) return igemm_tf32_mtiles(g, max_px);
   if (a_path == 1) return igemm_patch_mtiles(g, max_px);
   return tma_shape(g, max_px).box.boxes;
 }
 
 int igemm_tc_chunks(const ConvGeom& g, int a_path, int tile_n) {
+  if (g.dtype == FCONV_F32) return igemm_tf32_chunks(g);
   if (a_path == 1) return igemm_patch_chunks(g, tile_n);
   return (g.Kg + kBK - 1) / kBK;
 }
 
 int launch_igemm_tc(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& a, void* stream) {
+  if (g.dtype == FCONV_F32) return launch_igemm_tf32(g, c, a, stream);
   if (c.a_path == 1) return launch_igemm_patch(g, c, a, stream);
   return launch_tma_path(g, c, a, (cudaStream_t)stream);
 }
 
 int read_and_clear_device_error(void* stream, unsigned* value) {
-  unsigned v1 = 0, v2 = 0, v3 = 0, v4 = 0;
+  unsigned v1 = 0, v2 = 0, v3 = 0, v4 = 0, v5 = 0;
   int e = read_and_clear_tc_error((cudaStream_t)stream, &v1);
   if (e != 0) return e;
   e = read_and_clear_patch_error(stream, &v2);
@@ -642,7 +650,9 @@ int read_and_clear_device_error(void* stream, unsigned* value) {
   if (e != 0) return e;
   e = read_and_clear_dw_error(stream, &v4);
   if (e != 0) return e;
-  *value = v1 | v2 | v3 | v4;
+  e = read_and_clear_tf32_error(stream, &v5);
+  if (e != 0) return e;
+  *value = v1 | v2 | v3 | v4 | v5;
   return 0;
 }
 

@@ -171,6 +171,15 @@ def compute_peak(bound, peaks):
     return peaks["alu_f32_tflops"] if bound == "alu" else peaks["bf16_tflops"]
 
 
+# fp32 convolutions on the tensor cores issue three TF32 MMAs per product (3xTF32 split): their
+# peak is the TF32 rate (the measured bf16 rate x the nominal TF32/bf16 ratio 1.1/2.25) / 3.
+TF32_OVER_BF16 = 1.1 / 2.25
+
+
+def tf32x3_peak(peaks):
+    return peaks["bf16_tflops"] * TF32_OVER_BF16 / 3.0
+
+
 def main_kernel_name(case, route):
     """The kernel that does the conv's arithmetic (the TMA-fed implicit GEMM takes
     C/group a multiple of 64; other tensor-core convs build A from the input patch)."""
@@ -216,6 +225,40 @@ def measure_next_rows(dev, stream, flush, peaks):
                      "gbs": round(plan.bytes / (ms * 1e-3) / 1e9, 1), "bound": bnd,
                      "frac_of_bound": round(frac, 4), "flops": plan.flops,
                      "bytes": plan.bytes, "kernel": "convt_kernel"})
+    for case in workloads.FP32_TC_CASES:
+        t = workloads.make_inputs(case, fc.FusedConvPlan(
+            _lib.F32, case.x_shape, case.w_shape, has_bias=case.has_bias, has_z=case.has_z,
+            **case.attrs()).y_shape)
+        d = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in t.items()}
+        res = {}
+        for route, reps in (("auto", 10), ("direct", 3)):
+            plan = fc.FusedConvPlan(_lib.F32, case.x_shape, case.w_shape, has_bias=True,
+                                    has_z=True, route=route, **case.attrs())
+            y = torch.empty(plan.y_shape, dtype=torch.float32, device=dev)
+            wsb = (torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+                   if plan.workspace_bytes else None)
+            for _ in range(2):
+                plan.run(d["x"], d["w"], d["b"], d["z"], y=y, workspace=wsb, stream=stream)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(reps)]
+            for a, b in ev:
+                flush.zero_()
+                a.record(stream)
+                plan.run(d["x"], d["w"], d["b"], d["z"], y=y, workspace=wsb, stream=stream)
+                b.record(stream)
+            torch.cuda.synchronize()
+            res[route] = (plan, sum(a.elapsed_time(b) for a, b in ev) / reps)
+        plan, ms = res["auto"]
+        tf = plan.flops / (ms * 1e-3) / 1e12
+        pk = tf32x3_peak(peaks)
+        rows.append({"row": "NEXT-1 fp32 on the tensor cores (3xTF32)", "conv": case.name,
+                     "route": plan.route, "launches": plan.launches, "us": round(ms * 1e3, 2),
+                     "tflops": round(tf, 2), "bound": "tensor", "peak_tflops": round(pk, 1),
+                     "peak_kind": "measured bf16 x nominal TF32/bf16 (1.1/2.25) / 3 MMAs",
+                     "frac_of_bound": round(tf / pk, 4), "flops": plan.flops,
+                     "kernel": "igemm_tf32_kernel",
+                     "cuda_core_route_us": round(res["direct"][1] * 1e3, 2),
+                     "speedup_vs_cuda_cores": round(res["direct"][1] / ms, 1)})
     return rows
 
 

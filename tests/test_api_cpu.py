@@ -280,3 +280,22 @@ def test_launch_counts_and_workspace_regions(lib):
     c1 = workloads.case_by_name("2d_f32_3to8_k3_relu")
     p1 = FusedConvPlan(_lib.F32, c1.x_shape, c1.w_shape, has_bias=True, **c1.attrs())
     assert p1.route == "direct" and p1.launches == 1 and p1.workspace_bytes == 0
+
+
+def test_fp32_tensor_core_plans(lib):
+    # C/group a multiple of 32: the 3xTF32 tensor-core path (prologue, GEMM, reduce)
+    p = FusedConvPlan(_lib.F32, (2, 64, 10, 10), (48, 64, 3, 3), pads=[1, 1, 1, 1])
+    assert p.route == "igemm_tc" and p.launches == 3
+    kg, xs = 64 * 9, 2 * 64 * 100
+    r = lambda v: (v + 1023) // 1024 * 1024
+    assert p.workspace_bytes == 2 * r(48 * kg * 4) + 2 * r(xs * 4) + p.split_k * 2 * 48 * 100 * 4
+    # forced split and pixel tile
+    p = FusedConvPlan(_lib.F32, (2, 64, 10, 10), (48, 64, 3, 3), pads=[1, 1, 1, 1],
+                      split_k=3, tile_n=64)
+    assert (p.split_k, p.tile_n) == (3, 64)
+    # C/group not a multiple of 32 stays on CUDA cores; the patch-fed A path is f16 only
+    assert FusedConvPlan(_lib.F32, (2, 48, 10, 10), (16, 48, 3, 3)).route == "direct"
+    with pytest.raises(FconvError):
+        FusedConvPlan(_lib.F32, (2, 64, 10, 10), (48, 64, 3, 3), route="igemm_tc",
+                      a_path="gather")
+

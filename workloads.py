@@ -207,3 +207,13 @@ def make_transposed_inputs(case: dict, y_shape: Sequence[int]) -> dict:
             "w": draw(s + 1, ws, "normal", 1.0 / float(np.sqrt(kg)), dt),
             "b": draw(s + 2, (y_shape[1],), "normal", 1.0, dt),
             "z": draw(s + 3, y_shape, "normal", 1.0, dt)}
+
+
+# fp32 convolution on the tensor cores (3xTF32): a ResNet-stage 3x3 conv, measured beside the
+# suite with the CUDA-core route timed on the same inputs for comparison.
+FP32_TC_CASES = [
+    ConvCase("f32_tc_128to128_28x28_k3", "f32", (32, 128, 28, 28), (128, 128, 3, 3),
+             has_bias=True, has_z=True, pads=(1, 1, 1, 1), activation="Relu",
+             w_dist=("normal", 0.03), workload=6, conv_index=0),
+]
+
