@@ -57,7 +57,7 @@ class FusedConvPlan:
                  activation: Optional[str] = None, activation_params=None, device: int = -1,
                  route: str = "auto", split_k: int = 0, tile_n: int = 0, z_shape=None,
                  a_path: str = "auto", max_ctas: int = 0, transposed: bool = False,
-                 output_padding=None):
+                 output_padding=None, precision: str = "default"):
         lib = _lib.load()
         self._lib = lib
         self._ptr = ctypes.c_void_p()
@@ -95,7 +95,9 @@ class FusedConvPlan:
                               activation_params=activation_params, transposed=transposed,
                               output_padding=output_padding)
         opts = _lib.FconvOptions(ROUTES[route], int(split_k), int(tile_n),
-                                 {"auto": 0, "gather": 1, "tma": 2}[a_path], int(max_ctas))
+                                 {"auto": 0, "gather": 1, "tma": 2}[a_path], int(max_ctas),
+                                 _lib.PRECISIONS[precision])
+        self.precision = precision
         _check(lib.fconv_plan_create_ex(ctypes.byref(desc), device, ctypes.byref(opts),
                                         ctypes.byref(self._ptr)), "fconv_plan_create")
         ys = (ctypes.c_int64 * 5)()

@@ -15,6 +15,7 @@ ACTIVATIONS = {None: 0, "Relu": 1, "LeakyRelu": 2, "Sigmoid": 3, "Tanh": 4, "Har
 ROUTES = {"auto": 0, "direct": 1, "igemm_tc": 2, "depthwise": 3, "grouped": 4,
           "transposed": 5}
 ROUTE_NAMES = {v: k for k, v in ROUTES.items()}
+PRECISIONS = {"default": 0, "half2_rows": 1}
 STATUS = {0: "OK", 1: "E_NULL", 2: "E_RANK", 3: "E_ATTR_LENGTH", 4: "E_ATTR_VALUE",
           5: "E_PADS_WITH_AUTOPAD", 6: "E_KERNEL_SHAPE", 7: "E_GROUP", 8: "E_BIAS_SHAPE",
           9: "E_Z_SHAPE", 10: "E_ACT_PARAMS", 11: "E_ACTIVATION", 12: "E_OUTPUT_EMPTY",
@@ -42,7 +43,8 @@ class FconvDesc(ctypes.Structure):
 
 class FconvOptions(ctypes.Structure):
     _fields_ = [("route", ctypes.c_int), ("split_k", ctypes.c_int), ("tile_n", ctypes.c_int),
-                ("a_path", ctypes.c_int), ("max_ctas", ctypes.c_int)]
+                ("a_path", ctypes.c_int), ("max_ctas", ctypes.c_int),
+                ("precision", ctypes.c_int)]
 
 
 EXPORTS = ["fconv_plan_create", "fconv_plan_create_ex", "fconv_plan_output_shape",

@@ -258,6 +258,12 @@ fconv_status create(const fconv_desc* d, int device, const fconv_options* o, fco
     return FCONV_E_UNSUPPORTED;
   }
   p->g.max_ctas = o ? o->max_ctas : 0;
+  p->g.precision = o ? o->precision : FCONV_PRECISION_DEFAULT;
+  if (p->g.precision != FCONV_PRECISION_DEFAULT &&
+      (p->g.precision != FCONV_PRECISION_HALF2_ROWS || !depthwise_half2_supported(p->g))) {
+    delete p;
+    return FCONV_E_UNSUPPORTED;
+  }
   const fconv_route want = o ? o->route : FCONV_ROUTE_AUTO;
   fconv_route route = want;
   const int tile_n = (o && o->tile_n) ? o->tile_n : kDefaultPixelTile;
@@ -289,6 +295,9 @@ fconv_status create(const fconv_desc* d, int device, const fconv_options* o, fco
     // includes FCONV_ROUTE_TRANSPOSED for a direct convolution
     st = FCONV_E_UNSUPPORTED;
   }
+  // the half2 mode exists on the depthwise kernel only
+  if (st == FCONV_OK && p->g.precision != FCONV_PRECISION_DEFAULT && route != FCONV_ROUTE_DEPTHWISE)
+    st = FCONV_E_UNSUPPORTED;
   if (st == FCONV_OK && route == FCONV_ROUTE_IGEMM_TC && o && o->tile_n &&
       o->tile_n != 64 && o->tile_n != 128 && o->tile_n != 256)
     st = FCONV_E_UNSUPPORTED;

@@ -33,6 +33,7 @@ struct ConvGeom {
   int Kg;                       // Cg*KV
   int max_ctas;                 // cap on persistent CTAs (0 = none)
   int transposed;               // transposed convolution (W is (C, M/group, kernel...))
+  int precision;                // fconv_precision
 };
 
 struct ConvArgs {
@@ -58,6 +59,7 @@ struct IgemmConfig {
 int launch_direct(const ConvGeom& g, const ConvArgs& a, void* stream);
 int launch_depthwise(const ConvGeom& g, const ConvArgs& a, void* stream);
 bool depthwise_supported(const ConvGeom& g);
+bool depthwise_half2_supported(const ConvGeom& g);
 int read_and_clear_dw_error(void* stream, unsigned* value);
 int launch_grouped(const ConvGeom& g, const ConvArgs& a, void* stream);
 bool grouped_supported(const ConvGeom& g);

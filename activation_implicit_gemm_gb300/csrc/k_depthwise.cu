@@ -329,6 +329,61 @@ __device__ __forceinline__ void dw_strip(const T* box, int BW, const float (&wr)
   }
 }
 
+// Half2 row partials (opt-in precision mode, f16 only): for each kernel row the K taps of
+// two adjacent outputs are summed with packed f16 FMAs (each rounded once to f16), and the
+// row's two partial pairs are then added to the f32 accumulators. Against the f32 path this
+// trades K FMAs of error per kernel row (at most K * 2^-11 * sum |x*w| over the row) for
+// half the FMA instructions. The pair of outputs (j, j + 1) at tap kx needs the inputs
+// (j + kx + OFF, j + kx + OFF + 1): from the 16 halves of the row read as 8 words, an even
+// start is one word and an odd start a byte permute of two.
+__device__ __forceinline__ uint32_t prmt_b32(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+template <int K, int TH, int OFF>
+__device__ __forceinline__ void dw_strip_h2(const __half* box, int BW, const uint32_t (&wh)[K * K],
+                                            float (&acc)[TH][4]) {
+#pragma unroll
+  for (int r = 0; r < TH + K - 1; ++r) {
+    uint32_t wv[8];
+    const uint2* rp = reinterpret_cast<const uint2*>(box + r * BW);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint2 q = rp[i];
+      wv[2 * i] = q.x;
+      wv[2 * i + 1] = q.y;
+    }
+    uint32_t pr[K + 2];  // pr[t] = (x[OFF + t], x[OFF + t + 1])
+#pragma unroll
+    for (int t = 0; t < K + 2; ++t) {
+      const int s0 = OFF + t;
+      pr[t] = (s0 % 2 == 0) ? wv[s0 / 2] : prmt_b32(wv[s0 / 2], wv[s0 / 2 + 1], 0x5432u);
+    }
+#pragma unroll
+    for (int o = 0; o < TH; ++o) {
+      const int ky = r - o;
+      if (ky < 0 || ky >= K) continue;
+      __half2 p0 = __hmul2(*reinterpret_cast<const __half2*>(&pr[0]),
+                           *reinterpret_cast<const __half2*>(&wh[ky * K]));
+      __half2 p1 = __hmul2(*reinterpret_cast<const __half2*>(&pr[2]),
+                           *reinterpret_cast<const __half2*>(&wh[ky * K]));
+#pragma unroll
+      for (int kx = 1; kx < K; ++kx) {
+        const __half2 w2 = *reinterpret_cast<const __half2*>(&wh[ky * K + kx]);
+        p0 = __hfma2(*reinterpret_cast<const __half2*>(&pr[kx]), w2, p0);
+        p1 = __hfma2(*reinterpret_cast<const __half2*>(&pr[kx + 2]), w2, p1);
+      }
+      const float2 f0 = __half22float2(p0), f1 = __half22float2(p1);
+      acc[o][0] += f0.x;
+      acc[o][1] += f0.y;
+      acc[o][2] += f1.x;
+      acc[o][3] += f1.y;
+    }
+  }
+}
+
 // + Z, activation, rounding and the stores of a strip (rows past OH and columns past OW
 // are not stored).
 template <int ACT, typename T, int TH>
@@ -391,7 +446,7 @@ __device__ __forceinline__ DwUnit dw_unit(const DwTileArgs& a, int N, int u) {
   return r;
 }
 
-template <typename T, int K, int TH>
+template <typename T, int K, int TH, bool H2>
 __global__ void __launch_bounds__(kDwTileThreads, 2)
     dw_tile_kernel(const ConvGeom g, const DwTileArgs a, const T* __restrict__ w,
                    const T* __restrict__ b, const T* __restrict__ z, T* __restrict__ y,
@@ -456,10 +511,13 @@ __global__ void __launch_bounds__(kDwTileThreads, 2)
   const int cg = lt % a.ncg, strip = lt / a.ncg;
   const int off = a.a_off & 3;
   int wc = -1;
-  float wr[K * K];
+  float wr[H2 ? 1 : K * K];
+  uint32_t wh[H2 ? K * K : 1];  // half2 (w, w) per tap in the half2 mode
   float bias = 0.0f;
 #pragma unroll
-  for (int i = 0; i < K * K; ++i) wr[i] = 0.0f;
+  for (int i = 0; i < (H2 ? 1 : K * K); ++i) wr[i] = 0.0f;
+#pragma unroll
+  for (int i = 0; i < (H2 ? K * K : 1); ++i) wh[i] = 0u;
   int it = 0;
   for (int q = q0; q < q1; ++q, ++it) {
     const int s = it % kDwStages;
@@ -472,8 +530,16 @@ __global__ void __launch_bounds__(kDwTileThreads, 2)
       if (ox < g.OW && oy < g.OH) {
         if (un.c != wc) {
           wc = un.c;
+          if constexpr (H2) {
 #pragma unroll
-          for (int i = 0; i < K * K; ++i) wr[i] = to_f32(w[(long long)un.c * K * K + i]);
+            for (int i = 0; i < K * K; ++i) {
+              const __half2 h2 = __half2half2(*reinterpret_cast<const __half*>(&w[(long long)un.c * K * K + i]));
+              wh[i] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < K * K; ++i) wr[i] = to_f32(w[(long long)un.c * K * K + i]);
+          }
           bias = b ? to_f32(b[un.c]) : 0.0f;
         }
         const uint8_t* unit = dsm + (size_t)s * a.stage_bytes + (size_t)pp * a.unit_bytes;
@@ -483,11 +549,21 @@ __global__ void __launch_bounds__(kDwTileThreads, 2)
         for (int o = 0; o < TH; ++o)
 #pragma unroll
           for (int j = 0; j < 4; ++j) acc[o][j] = bias;
-        switch (off) {
-          case 0: dw_strip<T, K, TH, 0>(xb, a.BW, wr, acc); break;
-          case 1: dw_strip<T, K, TH, 1>(xb, a.BW, wr, acc); break;
-          case 2: dw_strip<T, K, TH, 2>(xb, a.BW, wr, acc); break;
-          default: dw_strip<T, K, TH, 3>(xb, a.BW, wr, acc); break;
+        if constexpr (H2) {
+          const __half* xh = reinterpret_cast<const __half*>(xb);
+          switch (off) {
+            case 0: dw_strip_h2<K, TH, 0>(xh, a.BW, wh, acc); break;
+            case 1: dw_strip_h2<K, TH, 1>(xh, a.BW, wh, acc); break;
+            case 2: dw_strip_h2<K, TH, 2>(xh, a.BW, wh, acc); break;
+            default: dw_strip_h2<K, TH, 3>(xh, a.BW, wh, acc); break;
+          }
+        } else {
+          switch (off) {
+            case 0: dw_strip<T, K, TH, 0>(xb, a.BW, wr, acc); break;
+            case 1: dw_strip<T, K, TH, 1>(xb, a.BW, wr, acc); break;
+            case 2: dw_strip<T, K, TH, 2>(xb, a.BW, wr, acc); break;
+            default: dw_strip<T, K, TH, 3>(xb, a.BW, wr, acc); break;
+          }
         }
         const T* zs = reinterpret_cast<const T*>(unit + a.z_off) + (strip * TH) * a.TWo + 4 * cg;
         const long long obase = ((long long)un.n * g.C + un.c) * g.P;
@@ -602,9 +678,10 @@ int launch_dw_tile(const ConvGeom& g, const DwTilePlan& p, const ConvArgs& args,
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int threads = (a.PP * a.tpu + 31) / 32 * 32 + 32;  // compute warps + the load warp
+  const bool h2 = g.precision == FCONV_PRECISION_HALF2_ROWS;
 #define FCONV_DW_TILE(KV, THV)                                                                  \
   if (g.KW == KV && p.TH == THV) {                                                              \
-    auto k = dw_tile_kernel<T, KV, THV>;                                                        \
+    auto k = h2 ? dw_tile_kernel<T, KV, THV, sizeof(T) == 2> : dw_tile_kernel<T, KV, THV, false>; \
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,         \
                                          (int)p.smem);                                          \
     if (e != cudaSuccess) return (int)e;                                                        \
@@ -677,6 +754,7 @@ int launch_dw_t(const ConvGeom& g, const ConvArgs& a, cudaStream_t s) {
   {
     const DwTilePlan tp = dw_tile_plan(g);
     if (tp.ok) return launch_dw_tile<T>(g, tp, a, s);
+    if (g.precision != FCONV_PRECISION_DEFAULT) return (int)cudaErrorInvalidValue;
   }
   if (unit && g.KH == g.KW && (g.KW == 3 || g.KW == 5 || g.KW == 7)) {
     // output tile: TC columns (<= 64, a multiple of 4), TR rows, at most 256 threads
@@ -713,6 +791,10 @@ bool depthwise_supported(const ConvGeom& g) {
   const long long blocks = (long long)g.N * g.C * dw_shape(g).bands;
   if (blocks > 0x7fffffffLL) return false;
   return dw_shape(g).smem <= (size_t)kDwMaxSmem;
+}
+
+bool depthwise_half2_supported(const ConvGeom& g) {
+  return g.dtype == FCONV_F16 && depthwise_supported(g) && dw_tile_plan(g).ok;
 }
 
 int read_and_clear_dw_error(void* stream, unsigned* value) {

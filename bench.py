@@ -225,6 +225,37 @@ def measure_next_rows(dev, stream, flush, peaks):
                      "gbs": round(plan.bytes / (ms * 1e-3) / 1e9, 1), "bound": bnd,
                      "frac_of_bound": round(frac, 4), "flops": plan.flops,
                      "bytes": plan.bytes, "kernel": "convt_kernel"})
+    # the opt-in half2 row-partial mode of the depthwise kernel on the stem's depthwise conv
+    case = workloads.case_by_name("stem_dw_128_k7")
+    times = {}
+    for prec in ("default", "half2_rows"):
+        plan = fc.FusedConvPlan(_lib.F16, case.x_shape, case.w_shape, has_bias=case.has_bias,
+                                has_z=case.has_z, precision=prec, **case.attrs())
+        if prec == "default":
+            t = workloads.make_inputs(case, plan.y_shape)
+            d = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in t.items()}
+            y = torch.empty(plan.y_shape, dtype=torch.float16, device=dev)
+        for _ in range(3):
+            plan.run(d["x"], d["w"], d["b"], d["z"], y=y, stream=stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(10)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            plan.run(d["x"], d["w"], d["b"], d["z"], y=y, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        times[prec] = (plan, sum(a.elapsed_time(b) for a, b in ev) / 10)
+    plan, ms = times["half2_rows"]
+    tf = plan.flops / (ms * 1e-3) / 1e12
+    rows.append({"row": "NEXT-2 half2 row partials (depthwise, opt-in precision)",
+                 "conv": case.name, "route": plan.route, "us": round(ms * 1e3, 2),
+                 "tflops": round(tf, 2), "gbs": round(plan.bytes / (ms * 1e-3) / 1e9, 1),
+                 "frac_of_hbm": round(plan.bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                 "default_precision_us": round(times["default"][1] * 1e3, 2),
+                 "speedup_vs_default": round(times["default"][1] / ms, 3),
+                 "kernel": "dw_tile_kernel<__half, 7, 7, true>",
+                 "error": "bounded by f16 rounding + 7 * 2^-11 * sum|x*w| (tests/test_gpu_half2.py)"})
     for case in workloads.FP32_TC_CASES:
         t = workloads.make_inputs(case, fc.FusedConvPlan(
             _lib.F32, case.x_shape, case.w_shape, has_bias=case.has_bias, has_z=case.has_z,

@@ -149,6 +149,17 @@ typedef struct {
   int64_t output_padding[3];
 } fconv_desc;
 
+/* Arithmetic modes. FCONV_PRECISION_HALF2_ROWS (opt-in, f16 2-D depthwise convs on the
+ * tiled depthwise kernel only; other requests return FCONV_E_UNSUPPORTED): the taps of each
+ * kernel row are summed for two adjacent outputs with packed f16 FMAs (each rounded once to
+ * f16) and the row partials are added in f32. Its error is bounded by the f16 output
+ * rounding plus K * 2^-11 * sum|x*w| (K taps per row), outside the default f16 tolerance
+ * (2e-3*|ref| + 1e-3*sum|x*w|/sqrt(Kg)); it takes fewer instructions per output. */
+typedef enum {
+  FCONV_PRECISION_DEFAULT = 0,
+  FCONV_PRECISION_HALF2_ROWS = 1
+} fconv_precision;
+
 /* Planner overrides, for tests and experiments. Zero-initialise for defaults. */
 typedef struct {
   fconv_route route;            /* FCONV_ROUTE_AUTO = choose */
@@ -162,6 +173,7 @@ typedef struct {
   int max_ctas;                 /* 0 = as many persistent CTAs as the work and the SMs allow;
                                    else at most this many (the persistent kernels then walk
                                    more work units per CTA) */
+  int precision;                /* fconv_precision (0 = the default: f32 accumulation) */
 } fconv_options;
 
 typedef struct fconv_plan fconv_plan;

@@ -299,3 +299,19 @@ def test_fp32_tensor_core_plans(lib):
         FusedConvPlan(_lib.F32, (2, 64, 10, 10), (48, 64, 3, 3), route="igemm_tc",
                       a_path="gather")
 
+
+
+def test_half2_precision_is_depthwise_f16_only(lib):
+    dw = dict(group=8, pads=[3, 3, 3, 3])
+    p = FusedConvPlan(_lib.F16, (2, 8, 24, 24), (8, 1, 7, 7), precision="half2_rows", **dw)
+    assert p.route == "depthwise"
+    bad = [
+        ((_lib.F32, (2, 8, 24, 24), (8, 1, 7, 7)), dw),                   # f32
+        ((_lib.F16, (2, 8, 24, 24), (16, 8, 3, 3)), dict(pads=[1, 1, 1, 1])),  # not depthwise
+        ((_lib.F16, (2, 8, 24, 21), (8, 1, 7, 7)), dw),                   # rows not 16-byte
+        ((_lib.F16, (2, 8, 24, 24), (8, 1, 7, 7)), dict(dw, route="direct")),
+    ]
+    for (dt, xs, ws), attrs in bad:
+        with pytest.raises(FconvError) as e:
+            FusedConvPlan(dt, xs, ws, precision="half2_rows", **attrs)
+        assert e.value.code == "E_UNSUPPORTED"
