@@ -81,6 +81,7 @@ struct PatchArgs {
   int mpad;                // resident weights: rows per group (ntiles * 128)
   uint32_t res_bytes;
   int R, Mp;               // stacked sub-boxes and the lanes of each (Mp = 128 / R)
+  int pairs;               // taps (kx, kx+1) are adjacent, 4-byte aligned halves: 32-bit gathers
 };
 
 struct PatchCtl {
@@ -331,6 +332,35 @@ __global__ void __launch_bounds__(kPThreads, 1)
           // two units per step, their table entries shared by this thread's rows: the loads
           // of both units and rows are independent and in flight together
           const int* tk = tab + kin;
+          if (a.pairs) {
+            // stride == kernel along x (even stride, even kernel width, dilation 1, even left
+            // pad): the taps kx, kx + 1 of a pixel are neighbours in the patch and the pair
+            // starts on a 4-byte boundary, so one 32-bit load brings two k values already in
+            // the order the row wants (len is even: K per block is a multiple of KW)
+#pragma unroll 1
+            for (int uu = 0; uu < nunits; uu += 2) {
+              const int k0 = 8 * uu;
+              const int4 t0 = *reinterpret_cast<const int4*>(tk + k0);
+              const int4 t1 = *reinterpret_cast<const int4*>(tk + k0 + 4);
+              const int4 t2 = *reinterpret_cast<const int4*>(tk + k0 + 8);
+              const int4 t3 = *reinterpret_cast<const int4*>(tk + k0 + 12);
+              const bool full = k0 + 16 <= len;
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                if (h >= nrow || !row_ok[h]) continue;
+                const uint32_t src = pslot + 2u * (uint32_t)(rbase[h] + ao);
+                auto ldp = [&](int off, int j) -> uint32_t {
+                  return (full || k0 + 2 * j < len) ? ptx::ld_shared_u32(src + off) : 0u;
+                };
+                const uint32_t e0 = ldp(t0.x, 0), e1 = ldp(t0.z, 1), e2 = ldp(t1.x, 2), e3 = ldp(t1.z, 3);
+                const uint32_t f0 = ldp(t2.x, 4), f1 = ldp(t2.z, 5), f2 = ldp(t3.x, 6), f3 = ldp(t3.z, 7);
+                const uint32_t arow = stg + roff[h];
+                const uint32_t swz = (roff[h] >> 7) & 7u;
+                ptx::st_shared_v4(arow + (((uint32_t)uu ^ swz) << 4), e0, e1, e2, e3);
+                ptx::st_shared_v4(arow + (((uint32_t)(uu + 1) ^ swz) << 4), f0, f1, f2, f3);
+              }
+            }
+          } else
 #pragma unroll 1
           for (int uu = 0; uu < nunits; uu += 2) {
             const int k0 = 8 * uu;
@@ -590,7 +620,10 @@ PatchPlan patch_plan(const ConvGeom& g, int max_px) {
     if (p.box.rows > p.R * px || !patch_extents(g, p)) continue;
     // a smaller instantiation holds the box
     if (px > 64 && p.box.rows <= p.R * px / 2) continue;
-    for (int cb = cb_hi; cb >= 1; cb -= (g.Cg < 8 ? g.Cg : 8)) {
+    // blocks of C/group below 8: all of them, or (when a block's K stays a multiple of 8
+    // elements, as the weight boxes need) fewer, down to one channel per patch
+    for (int cb = cb_hi; cb >= 1; cb -= (g.Cg < 8 ? 1 : 8)) {
+      if (g.Cg < 8 && cb != g.Cg && (cb * g.KV) % 8 != 0) continue;
       p.Cb = cb;
       p.nblk = (g.Cg + cb - 1) / cb;
       p.Kb_full = cb * g.KV;
@@ -620,7 +653,6 @@ PatchPlan patch_plan(const ConvGeom& g, int max_px) {
         p.ok = true;
         return p;
       }
-      if (g.Cg < 8) break;
     }
   }
   return p;
@@ -721,6 +753,7 @@ int launch_igemm_patch(const ConvGeom& g, const IgemmConfig& c, const ConvArgs& 
   pa.mpad = p.mpad;
   pa.res_bytes = p.res_bytes;
   pa.R = p.R;
+  pa.pairs = (g.sW % 2 == 0 && g.KW % 2 == 0 && g.dW == 1 && g.pW % 2 == 0) ? 1 : 0;
   pa.Mp = kMT / p.R;
   const bool sp = c.split_k > 1;
   int err;

@@ -256,6 +256,42 @@ def measure_next_rows(dev, stream, flush, peaks):
                  "speedup_vs_default": round(times["default"][1] / ms, 3),
                  "kernel": "dw_tile_kernel<__half, 7, 7, true>",
                  "error": "bounded by f16 rounding + 7 * 2^-11 * sum|x*w| (tests/test_gpu_half2.py)"})
+    for case in workloads.PATCHIFY_CASES:
+        y_shape = fc.FusedConvPlan(_lib.F16, case.x_shape, case.w_shape, has_bias=case.has_bias,
+                                   has_z=case.has_z, **case.attrs()).y_shape
+        t = workloads.make_inputs(case, y_shape)
+        d = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).to(dev))
+             for k, v in t.items()}
+        res = {}
+        for route, reps in (("auto", 10), ("direct", 2)):
+            plan = fc.FusedConvPlan(_lib.F16, case.x_shape, case.w_shape, has_bias=case.has_bias,
+                                    has_z=case.has_z, route=route, **case.attrs())
+            y = torch.empty(plan.y_shape, dtype=torch.float16, device=dev)
+            wsb = (torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+                   if plan.workspace_bytes else None)
+            for _ in range(2):
+                plan.run(d["x"], d["w"], d["b"], d["z"], y=y, workspace=wsb, stream=stream)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(reps)]
+            for a, b in ev:
+                flush.zero_()
+                a.record(stream)
+                plan.run(d["x"], d["w"], d["b"], d["z"], y=y, workspace=wsb, stream=stream)
+                b.record(stream)
+            torch.cuda.synchronize()
+            res[route] = (plan, sum(a.elapsed_time(b) for a, b in ev) / reps)
+        plan, ms = res["auto"]
+        bnd = bound_of(plan.flops, plan.bytes, peaks, plan.route)
+        ach = (plan.flops / (ms * 1e-3) / 1e12 if bnd == "tensor"
+               else plan.bytes / (ms * 1e-3) / 1e9)
+        pk = peaks["bf16_tflops"] if bnd == "tensor" else peaks["hbm_gbs"]
+        rows.append({"row": "NEXT-3 stride == kernel (patchify)", "conv": case.name,
+                     "route": plan.route, "us": round(ms * 1e3, 2),
+                     "tflops": round(plan.flops / (ms * 1e-3) / 1e12, 2),
+                     "gbs": round(plan.bytes / (ms * 1e-3) / 1e9, 1), "bound": bnd,
+                     "frac_of_bound": round(ach / pk, 4), "kernel": "igemm_patch_kernel",
+                     "cuda_core_route_us": round(res["direct"][1] * 1e3, 2),
+                     "speedup_vs_cuda_cores": round(res["direct"][1] / ms, 1)})
     for case in workloads.FP32_TC_CASES:
         t = workloads.make_inputs(case, fc.FusedConvPlan(
             _lib.F32, case.x_shape, case.w_shape, has_bias=case.has_bias, has_z=case.has_z,

@@ -375,3 +375,28 @@ def test_config_full_size(name):
     alpha = (attrs.get("activation_params") or [1.0])[0]
     check(y, ref, absacc, c.dtype, kg, activation=attrs.get("activation"), alpha=alpha,
           what=f"{name} route={plan.route} split={plan.split_k}")
+
+
+# ----------------------------------------------------------------------------- stride == kernel
+# Even stride and even kernel width along x, dilation 1, even left pad: the patch-fed kernel's
+# builders read the taps (kx, kx + 1) of a pixel as one 32-bit load. An odd left pad keeps the
+# 2-byte gathers.
+PATCHIFY_CASES = [
+    ((2, 24, 16, 20), (40, 24, 2, 2), dict(strides=[2, 2]), {}),
+    ((1, 3, 64, 64), (32, 3, 4, 4), dict(strides=[4, 4], activation="Gelu"), {}),
+    ((2, 16, 40), (24, 16, 2), dict(strides=[2]), {}),
+    ((1, 8, 4, 8, 8), (16, 8, 2, 2, 2), dict(strides=[2, 2, 2]), {}),
+    ((2, 128, 14, 14), (256, 128, 2, 2), dict(strides=[2, 2]), dict(a_path="gather")),
+    ((2, 32, 12, 16), (48, 32, 2, 2), dict(strides=[2, 2], pads=[0, 2, 0, 2]), dict(split_k=2)),
+    ((2, 32, 12, 16), (48, 32, 2, 2), dict(strides=[2, 2], pads=[1, 1, 1, 1]), {}),  # odd pad
+    # patch embeddings of RGB images: one channel per patch block (its K stays a multiple of 8)
+    ((2, 3, 64, 64), (96, 3, 8, 8), dict(strides=[8, 8]), {}),
+    ((2, 3, 224, 224), (768, 3, 16, 16), dict(strides=[16, 16], activation="Gelu"), {}),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(PATCHIFY_CASES)))
+def test_stride_equals_kernel(idx):
+    xs, ws, attrs, opts = PATCHIFY_CASES[idx]
+    x, w, b, z = inputs(1900 + 10 * idx, "f16", xs, ws, True, True, attrs)
+    compare("f16", x, w, b, z, attrs, route="igemm_tc", what=f"patchify {idx}", **opts)

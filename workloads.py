@@ -217,3 +217,12 @@ FP32_TC_CASES = [
              w_dist=("normal", 0.03), workload=6, conv_index=0),
 ]
 
+
+# stride == kernel (patchify): a ViT patch embedding of RGB images, 16x16 patches, measured
+# beside the suite with the CUDA-core route timed on the same inputs for comparison.
+PATCHIFY_CASES = [
+    ConvCase("vit_patchify_3to768_k16_s16", "f16", (32, 3, 224, 224), (768, 3, 16, 16),
+             has_bias=True, strides=(16, 16), w_dist=("normal", 0.036), workload=7,
+             conv_index=0),
+]
+
