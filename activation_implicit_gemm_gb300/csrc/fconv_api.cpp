@@ -207,12 +207,29 @@ fconv_status resolve(const fconv_desc* d, fconv_plan* p) {
 
 // Largest pixel tile (MMA N) of the tensor-core kernels; channel tiles are always 128.
 constexpr int kDefaultPixelTile = 256;
+// FLOPs per HBM byte above which a GB300 conv is tensor-bound: the measured dense f16 GEMM
+// rate over the measured copy rate (1909 TFLOP/s / 6787 GB/s).
+constexpr double kRidgeFlopPerByte = 281.0;
 
 void plan_igemm(fconv_plan* p, const fconv_options* o) {
   const ConvGeom& g = p->g;
   IgemmConfig& c = p->igemm;
   c.tile_n = (o && o->tile_n) ? o->tile_n : kDefaultPixelTile;
   c.a_path = igemm_tc_resolve_path(g, c.tile_n, o ? o->a_path : 0);
+  if (!(o && o->tile_n) && c.a_path == 2 && g.dtype == FCONV_F16) {
+    // TMA-fed convs below the ridge (HBM-bound) run faster with more, smaller pixel tiles:
+    // measured on the suite, 256 -> 128 pixels took cnn B (64->128 @16) from 46 to 41 us and
+    // the stem downsample from 28 to 25 us, and 64 pixels took the 1-D conv (16 tiles of
+    // 256) from 24 to 13 us; the tensor-bound convs keep 256
+    const double flops = 2.0 * g.N * (double)g.M * (double)g.P * g.Kg;
+    const double bytes = 2.0 * ((double)g.N * g.C * (double)g.IS + (double)g.M * g.Kg +
+                                (double)g.N * g.M * (double)g.P * (g.has_z ? 2.0 : 1.0));
+    if (flops < kRidgeFlopPerByte * bytes) {
+      c.tile_n = 128;
+      const long long units = igemm_tc_mtiles(g, 2, 128) * ((g.Mg + 127) / 128) * g.G;
+      if (units * 2 < p->sms) c.tile_n = 64;
+    }
+  }
   const long long rows = igemm_tc_mtiles(g, c.a_path, c.tile_n);
   const long long tiles = rows * ((g.Mg + 127) / 128) * g.G;
   const int chunks = igemm_tc_chunks(g, c.a_path, c.tile_n);
