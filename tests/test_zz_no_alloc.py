@@ -146,3 +146,33 @@ def test_noalloc_runs_workspace_free_routes():
     ref, absacc = oracle.fused_conv(x, w, b, z, **attrs)
     check(y.double().cpu().numpy(), ref, absacc, "f16", 9, activation="Clip",
           what="noalloc depthwise")
+
+
+def test_noalloc_runs_the_fp32_tensor_core_path():
+    # the 3xTF32 plan's workspace holds W hi/lo, X hi/lo and the raw sums: all in the array
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    _build.build()
+    run_noalloc = noalloc_fn()
+    xs, wsh = (2, 32, 9, 9), (40, 32, 3, 3)
+    attrs = dict(pads=[1, 1, 1, 1], activation="Relu")
+    plan = FusedConvPlan(_lib.F32, xs, wsh, has_bias=True, has_z=True, **attrs)
+    assert plan.route == "igemm_tc" and 0 < plan.workspace_bytes <= SCRATCH_BYTES
+    ys = oracle.output_shape(xs, wsh, **attrs)
+    x = workloads.draw(71, xs, "normal", 1.0, "f32")
+    w = workloads.draw(72, wsh, "normal", 1.0 / math.sqrt(32 * 9), "f32")
+    b = workloads.draw(73, (40,), "normal", 1.0, "f32")
+    z = workloads.draw(74, ys, "normal", 1.0, "f32")
+    d = [torch.from_numpy(a).cuda() for a in (x, w, b, z)]
+    y_run = plan.run(*d)
+    torch.cuda.synchronize()
+    ref, absacc = oracle.fused_conv(x, w, b, z, **attrs)
+    for call in range(2):
+        y = torch.full(plan.y_shape, float("nan"), dtype=torch.float32, device="cuda")
+        st = run_noalloc(plan._ptr, *(t.data_ptr() for t in d), y.data_ptr(),
+                         torch.cuda.current_stream().cuda_stream)
+        assert _lib.STATUS[st] == "OK", f"call {call}: {_lib.STATUS[st]}"
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_run)
+        check(y.double().cpu().numpy(), ref, absacc, "f32", 32 * 9, activation="Relu",
+              what=f"noalloc tf32 call {call}")
