@@ -262,6 +262,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // box pixels i0 and i0 + 256 (when R * NPX > 256): sub-box i / NPX, row i % NPX
     const int i = (warp - kPBuildWarp0) * 32 + lane;
     const int nrow = (a.R * NPX + kPBuildThreads - 1) / kPBuildThreads;
+    // at most 128 rows a chunk: two threads per row, each writing half of its 16-byte units
+    const bool halves = a.R * NPX <= kPBuildThreads / 2;
+    const int ri = halves ? (i & (kPBuildThreads / 2 - 1)) : i;
+    const int half = halves ? (i / (kPBuildThreads / 2)) : 0;
     int rbase[2] = {0, 0};
     uint32_t roff[2] = {0u, 0u};
     bool row_ok[2] = {false, false};
@@ -271,7 +275,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     bool row_zero[2] = {false, false};
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int pi = i + h * kPBuildThreads;
+      const int pi = ri + h * kPBuildThreads;
       row_ok[h] = h < nrow && pi < a.t.rows;
       row_zero[h] = a.R > 1 && h < nrow && pi >= a.t.rows && pi < a.R * NPX;
       const int wt = pi % a.t.Wt, ht = (pi / a.t.Wt) % a.t.Ht, dt = (pi / (a.t.Wt * a.t.Ht)) % a.t.Dt;
@@ -323,11 +327,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
           const int kin = (i0 + k) * kBK;
           const int len = min(kBK, kb - kin);
           const int nunits = ((len + 15) >> 4) * 2;  // 16-byte units the MMAs read (even)
+          // this thread's units of its rows: all, or one (even-aligned) half
+          int u_lo = 0, u_hi = nunits;
+          if (halves) {
+            const int mid = ((nunits >> 1) + 1) & ~1;
+            u_lo = half ? mid : 0;
+            u_hi = half ? nunits : mid;
+          }
           const uint32_t stg = base + st.idx * a.stage_bytes + wst;
 #pragma unroll
           for (int h = 0; h < 2; ++h)
             if (row_zero[h])
-              for (int uu = 0; uu < nunits; ++uu)
+              for (int uu = u_lo; uu < u_hi; ++uu)
                 ptx::st_shared_v4(stg + roff[h] + (((uint32_t)uu ^ ((roff[h] >> 7) & 7u)) << 4), 0u, 0u, 0u, 0u);
           // two units per step, their table entries shared by this thread's rows: the loads
           // of both units and rows are independent and in flight together
@@ -338,7 +349,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             // starts on a 4-byte boundary, so one 32-bit load brings two k values already in
             // the order the row wants (len is even: K per block is a multiple of KW)
 #pragma unroll 1
-            for (int uu = 0; uu < nunits; uu += 2) {
+            for (int uu = u_lo; uu < u_hi; uu += 2) {
               const int k0 = 8 * uu;
               const int4 t0 = *reinterpret_cast<const int4*>(tk + k0);
               const int4 t1 = *reinterpret_cast<const int4*>(tk + k0 + 4);
@@ -362,7 +373,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
           } else
 #pragma unroll 1
-          for (int uu = 0; uu < nunits; uu += 2) {
+          for (int uu = u_lo; uu < u_hi; uu += 2) {
             const int k0 = 8 * uu;
             const int4 t0 = *reinterpret_cast<const int4*>(tk + k0);
             const int4 t1 = *reinterpret_cast<const int4*>(tk + k0 + 4);
