@@ -429,6 +429,163 @@ __device__ __forceinline__ void dw_strip_store(const ConvGeom& g, const DwTileAr
   }
 }
 
+// ------------------------------------------------------------------ column streaming
+// dw_stream_kernel: stride 1, dilation 1, K in {3, 5, 7}, rows of X and Y a multiple of 4
+// elements. A thread owns 4 adjacent output columns of one (n, c) plane over the plane's
+// whole height and walks the input rows top to bottom once: input row r - pH feeds the K
+// output rows r - K + 1 .. r, held as K rolling rows of 4 accumulators (slot s meets the
+// row with kernel row K - 1 - s). After a row, slot 0 is complete and leaves (+ Z,
+// activation, one rounding to T, one vector store); the slots move down by one and the
+// last is seeded with the bias. Each thread streams its input rows (4-element vectors,
+// zeros outside X, which is the padding) and Z rows through a private ring of asynchronous
+// copies into shared memory, kDwStreamAhead - 1 rows ahead of their use, so the loads are
+// in flight during the FMAs; no thread reads another's slots, so there is no barrier. The
+// loop body is one row (K*K*4 FMAs), small enough for the instruction cache. The tiled
+// kernel (below) covers the other shapes and the half2 mode.
+template <typename T>
+struct DwVec;
+template <>
+struct DwVec<__half> {
+  static constexpr uint32_t bytes = 8;
+  static __device__ __forceinline__ void copy(uint32_t dst, const void* src, uint32_t n) {
+    ptx::cp_async8(dst, src, n);
+  }
+  static __device__ __forceinline__ void read(uint32_t at, float* f) {
+    uint32_t lo, hi;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(lo), "=r"(hi) : "r"(at));
+    const __half2 l = *reinterpret_cast<const __half2*>(&lo);
+    const __half2 h = *reinterpret_cast<const __half2*>(&hi);
+    f[0] = __low2float(l); f[1] = __high2float(l);
+    f[2] = __low2float(h); f[3] = __high2float(h);
+  }
+};
+template <>
+struct DwVec<float> {
+  static constexpr uint32_t bytes = 16;
+  static __device__ __forceinline__ void copy(uint32_t dst, const void* src, uint32_t n) {
+    ptx::cp_async16(dst, src, n);
+  }
+  static __device__ __forceinline__ void read(uint32_t at, float* f) {
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3]) : "r"(at));
+  }
+};
+
+// One CTA of 384 threads per SM (at most): the columns are spread evenly over the SMs
+// whichever SMs free up first when the kernel starts behind another one.
+constexpr int kDwStreamThreads = 384;
+constexpr int kDwStreamAhead = 4;  // rows of X (and Z) in the ring per thread
+
+// 4-element vectors per input row. The ring of one CTA: slot (row % kDwStreamAhead,
+// vector q) of thread t at ((slot * (NQ + 1) + q) * kDwStreamThreads + t) * bytes (vector
+// q == NQ holds Z), so that a warp's reads of one vector are consecutive.
+template <typename T, int K, int OFF>
+__host__ __device__ constexpr int dw_stream_nq() { return (OFF + K + 3 + 3) / 4; }
+
+template <typename T, int K, int OFF, int ACT>
+__device__ __forceinline__ void dw_stream_column(const ConvGeom& g, const T* __restrict__ x,
+                                                 const T* __restrict__ w, const T* __restrict__ b,
+                                                 const T* __restrict__ z, T* __restrict__ y,
+                                                 long long plane, int t, uint32_t ring) {
+  using V = DwVec<T>;
+  constexpr int NQ = dw_stream_nq<T, K, OFF>();
+  constexpr int D = kDwStreamAhead;
+  const int c = (int)(plane % g.C);
+  float wr[K * K];
+#pragma unroll
+  for (int i = 0; i < K * K; ++i) wr[i] = to_f32(w[(long long)c * K * K + i]);
+  const float bias = b ? to_f32(b[c]) : 0.0f;
+  const int ox = 4 * t;
+  const int xs = ox - g.pW - OFF;  // column of the first vector (a multiple of 4)
+  bool cok[NQ];
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) cok[q] = xs + 4 * q >= 0 && xs + 4 * q < g.IW;
+  const T* xp = x + plane * (long long)g.IH * g.IW;
+  const long long ob = plane * (long long)g.OH * g.OW + ox;
+  const uint32_t me = ring + (uint32_t)threadIdx.x * V::bytes;
+  constexpr uint32_t kStep = kDwStreamThreads * V::bytes;  // one vector of every thread
+  const int rows = g.OH + K - 1;
+  // step r: input row r - pH, and Z of the output row r - (K - 1) that leaves at step r;
+  // zeros (nothing read) outside X, and for Z before the first output row or without Z
+  auto issue = [&](int r) {
+    const uint32_t slot = me + (uint32_t)((r % D) * (NQ + 1)) * kStep;
+    const int ir = r - g.pH;
+    const bool rok = r < rows && ir >= 0 && ir < g.IH;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      const bool ok = rok && cok[q];
+      V::copy(slot + (uint32_t)q * kStep,
+              ok ? (const void*)(xp + (long long)ir * g.IW + xs + 4 * q) : (const void*)x,
+              ok ? V::bytes : 0u);
+    }
+    const int o = r - (K - 1);
+    const bool zok = z != nullptr && r < rows && o >= 0;
+    V::copy(slot + (uint32_t)NQ * kStep,
+            zok ? (const void*)(z + ob + (long long)o * g.OW) : (const void*)x, zok ? V::bytes : 0u);
+    ptx::cp_async_commit();
+  };
+#pragma unroll
+  for (int r = 0; r < D - 1; ++r) issue(r);
+  float acc[K][4];
+#pragma unroll
+  for (int sl = 0; sl < K; ++sl)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[sl][j] = bias;
+#pragma unroll 1
+  for (int r = 0; r < rows; ++r) {
+    issue(r + D - 1);             // D - 1 rows ahead of this one
+    ptx::cp_async_wait<D - 1>();  // this step's group has landed
+    const uint32_t slot = me + (uint32_t)((r % D) * (NQ + 1)) * kStep;
+    float win[4 * NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) V::read(slot + (uint32_t)q * kStep, win + 4 * q);
+#pragma unroll
+    for (int kx = 0; kx < K; ++kx)
+#pragma unroll
+      for (int sl = 0; sl < K; ++sl) {
+        const float wv = wr[(K - 1 - sl) * K + kx];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[sl][j] = fmaf(win[OFF + j + kx], wv, acc[sl][j]);
+      }
+    const int o = r - (K - 1);  // the output row slot 0 completes now
+    if (o >= 0) {
+      float zv[4];
+      V::read(slot + (uint32_t)NQ * kStep, zv);
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        v[j] = act_eval<ACT, sizeof(T) == 2>(acc[0][j] + zv[j], g.alpha, g.beta);
+      store4(y + ob + (long long)o * g.OW, v);
+    }
+#pragma unroll
+    for (int sl = 0; sl < K - 1; ++sl)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[sl][j] = acc[sl + 1][j];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[K - 1][j] = bias;
+  }
+  ptx::cp_async_wait<0>();  // the ring's last (empty) groups, before the slots are reused
+}
+
+template <typename T, int K, int OFF>
+__global__ void __launch_bounds__(kDwStreamThreads, 1)
+    dw_stream_kernel(const ConvGeom g, int tpp, long long nthr, const T* __restrict__ x,
+                     const T* __restrict__ w, const T* __restrict__ b, const T* __restrict__ z,
+                     T* __restrict__ y) {
+  extern __shared__ __align__(16) uint8_t dws[];
+  const uint32_t ring = ptx::smem_addr(dws);
+  ptx::pdl_wait();  // inputs may be the previous kernel's outputs
+  ptx::pdl_trigger();
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x; gid < nthr; gid += stride) {
+    const long long plane = gid / tpp;
+    const int t = (int)(gid - plane * tpp);
+#define FCONV_DW_STREAM(ACT) dw_stream_column<T, K, OFF, ACT>(g, x, w, b, z, y, plane, t, ring)
+    FCONV_ACT_SWITCH(g.act, FCONV_DW_STREAM)
+#undef FCONV_DW_STREAM
+  }
+}
+
 // Unit u -> (channel, image, tile row, tile column).
 struct DwUnit {
   int c, n, th, tw;
@@ -741,6 +898,49 @@ __global__ void __launch_bounds__(kDwThreads) dw_kernel_generic(ConvGeom g, cons
   }
 }
 
+// The column-streaming kernel takes stride 1, dilation 1, K in {3, 5, 7} with the left pad
+// of a same-size conv modulo 4 ((K - 1) / 2, so that one vector offset per K is compiled),
+// rows of X and Y that are whole 4-element vectors, and vector-aligned X, Z and Y, in the
+// default precision.
+bool dw_stream_ok(const ConvGeom& g) {
+  if (!(g.Cg == 1 && g.Mg == 1 && g.KD == 1 && g.ID == 1 && g.OD == 1)) return false;
+  if (!(g.sW == 1 && g.dW == 1 && g.sH == 1 && g.dH == 1 && g.KH == g.KW)) return false;
+  if (g.KW != 3 && g.KW != 5 && g.KW != 7) return false;
+  if ((g.pW - (g.KW - 1) / 2) % 4 != 0) return false;
+  if (g.precision != FCONV_PRECISION_DEFAULT) return false;
+  if (g.N < 1 || g.C < 1 || g.OH < 1 || g.OW < 4) return false;
+  return g.IW % 4 == 0 && g.OW % 4 == 0 && (long long)g.N * g.C * (g.OW / 4) < 0x7fffffffLL * 128LL;
+}
+
+bool vec_aligned(const void* p, size_t bytes) { return p == nullptr || ((uintptr_t)p % bytes) == 0; }
+
+template <typename T>
+int launch_dw_stream(const ConvGeom& g, const ConvArgs& a, cudaStream_t s) {
+  const int tpp = g.OW / 4;
+  const long long nthr = (long long)g.N * g.C * tpp;
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long grid = (nthr + kDwStreamThreads - 1) / kDwStreamThreads;
+  if (grid > sms) grid = sms;
+  if (g.max_ctas > 0 && grid > g.max_ctas) grid = g.max_ctas;
+  const int off = ((-g.pW) % 4 + 4) % 4;
+#define FCONV_DW_STREAM_K(KV, OV)                                                              \
+  if (g.KW == KV && off == OV) {                                                               \
+    auto k = dw_stream_kernel<T, KV, OV>;                                                      \
+    const size_t smem = (size_t)kDwStreamAhead * (dw_stream_nq<T, KV, OV>() + 1) *             \
+                        kDwStreamThreads * DwVec<T>::bytes;                                    \
+    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,  \
+                                               (int)smem);                                       \
+    if (e != cudaSuccess) return (int)e;                                                        \
+    return launch_pdl(k, dim3((unsigned)grid), dim3(kDwStreamThreads), smem, s, g, tpp, nthr,   \
+                      (const T*)a.x, (const T*)a.w, (const T*)a.b, (const T*)a.z, (T*)a.y);     \
+  }
+  FCONV_DW_STREAM_K(3, 3) FCONV_DW_STREAM_K(5, 2) FCONV_DW_STREAM_K(7, 1)
+#undef FCONV_DW_STREAM_K
+  return (int)cudaErrorInvalidValue;
+}
+
 template <typename T>
 int launch_dw_t(const ConvGeom& g, const ConvArgs& a, cudaStream_t s) {
   const DwLaunch L = dw_shape(g);
@@ -751,6 +951,9 @@ int launch_dw_t(const ConvGeom& g, const ConvArgs& a, cudaStream_t s) {
   const T* z = (const T*)a.z;
   T* y = (T*)a.y;
   const bool unit = g.sW == 1 && g.dW == 1 && g.sH == 1 && g.dH == 1;
+  if (dw_stream_ok(g) && vec_aligned(a.x, 4 * sizeof(T)) && vec_aligned(a.z, 4 * sizeof(T)) &&
+      vec_aligned(a.y, 4 * sizeof(T)))
+    return launch_dw_stream<T>(g, a, s);
   {
     const DwTilePlan tp = dw_tile_plan(g);
     if (tp.ok) return launch_dw_tile<T>(g, tp, a, s);

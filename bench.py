@@ -216,13 +216,27 @@ def tf32x3_peak(peaks):
     return peaks["bf16_tflops"] * TF32_OVER_BF16 / 3.0
 
 
-def main_kernel_name(case, route):
+def dw_streams(case, plan) -> bool:
+    """Whether a depthwise plan runs the column-streaming kernel: 2-D, stride 1, dilation 1,
+    K in {3, 5, 7}, the same-size left pad modulo 4, rows of X and Y in whole 4-element
+    vectors, default precision (the library's rule; the bench's buffers are aligned)."""
+    if len(case.x_shape) != 4 or getattr(plan, "precision", "default") != "default":
+        return False
+    k = case.w_shape[-1]
+    ones = lambda v: v is None or all(e == 1 for e in v)
+    return (case.w_shape[-2] == k and k in (3, 5, 7) and ones(case.strides)
+            and ones(case.dilations) and (plan.pad_begin[2] - (k - 1) // 2) % 4 == 0
+            and case.x_shape[3] % 4 == 0 and plan.y_shape[3] % 4 == 0)
+
+
+def main_kernel_name(case, route, plan=None):
     """The kernel that does the conv's arithmetic (the TMA-fed implicit GEMM takes
     C/group a multiple of 64; other tensor-core convs build A from the input patch)."""
     if route == "igemm_tc":
         return "igemm_tma_kernel" if case.w_shape[1] % 64 == 0 else "igemm_patch_kernel"
-    return {"depthwise": "dw_tile_kernel", "direct": "direct_conv_kernel",
-            "grouped": "grouped_kernel"}[route]
+    if route == "depthwise":
+        return "dw_stream_kernel" if plan is not None and dw_streams(case, plan) else "dw_tile_kernel"
+    return {"direct": "direct_conv_kernel", "grouped": "grouped_kernel"}[route]
 
 
 def measure_next_rows(dev, stream, flush, peaks):
@@ -491,7 +505,7 @@ def run_ours(args):
     traffic = load_traffic(convs[top]["case"].name)
     roofline = {"bound": tb, "achieved": round(ach, 3), "peak": pk, "unit": unit,
                 "frac": round(ach / pk, 4), "traffic": traffic,
-                "kernel": main_kernel_name(convs[top]["case"], tp.route),
+                "kernel": main_kernel_name(convs[top]["case"], tp.route, tp),
                 "launch": convs[top]["case"].name,
                 "peak_kind": ("derived: 152 SMs x 128 f32 FMA lanes x 2 FLOP x max SM clock"
                               if tb == "alu" else f"{peaks_kind} (burst)"),

@@ -203,6 +203,16 @@ def test_activations(act, params, route):
     compare("f16", x, w, b, z, attrs, route=route, what=f"act {act}")
 
 
+@pytest.mark.parametrize("act,params", ACTS)
+def test_activations_dw_stream(act, params):
+    """Every activation through the column-streaming depthwise kernel (rows of X and Y in
+    whole 4-element vectors, stride 1, the same-size left pad)."""
+    xs, ws = (2, 8, 12, 16), (8, 1, 3, 3)
+    attrs = dict(pads=[1, 1, 1, 1], group=8, activation=act, activation_params=params)
+    x, w, b, z = inputs(520, "f16", xs, ws, True, True, attrs, wscale=0.8 / math.sqrt(9))
+    compare("f16", x, w, b, z, attrs, route="depthwise", what=f"dw stream act {act}")
+
+
 # ----------------------------------------------------------------------------- depthwise
 
 DW_CASES = [
@@ -223,7 +233,24 @@ DW_CASES = [
     ((2, 4, 19, 24), 7, dict(pads=[3, 0, 3, 0])),
     ((1, 3, 64, 136), 7, dict(auto_pad="SAME_UPPER")),
     ((2, 3, 12, 16), 3, dict(pads=[1, 3, 0, 3])),
+    # column streaming (widths in whole 4-element vectors, the same-size left pad): bottom
+    # and right pads other than the left and top ones, one column group, tall planes, pads
+    # wider than the kernel's half
+    ((2, 5, 21, 20), 5, dict(pads=[2, 2, 1, 2])),
+    ((1, 6, 9, 4), 3, dict(pads=[1, 1, 1, 1])),
+    ((1, 4, 130, 12), 7, dict(pads=[3, 3, 0, 3])),
+    ((2, 3, 16, 24), 7, dict(pads=[7, 7, 7, 7])),
 ]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "f32"])
+@pytest.mark.parametrize("k", [3, 5, 7])
+def test_depthwise_stream_without_b_z(k, dtype):
+    """The column-streaming kernel with neither bias nor residual."""
+    xs = (2, 6, 18, 20)
+    attrs = dict(group=6, pads=[(k - 1) // 2] * 4, activation="Relu")
+    x, w, b, z = inputs(760 + k, dtype, xs, (6, 1, k, k), False, False, attrs)
+    compare(dtype, x, w, b, z, attrs, route="depthwise", what=f"dw stream no b/z k={k}")
 
 
 @pytest.mark.parametrize("dtype", ["f16", "f32"])
@@ -330,6 +357,8 @@ EXACT_CASES = [
     ("f32", (2, 3, 5, 9, 8), (4, 3, 3, 3, 3), dict(strides=[1, 2, 1], auto_pad="SAME_UPPER"),
      "direct", {}, 2),
     ("f32", (2, 8, 14, 14), (8, 1, 3, 3), dict(group=8, pads=[1, 1, 1, 1]), "depthwise", {}, 2),
+    ("f16", (2, 8, 14, 16), (8, 1, 7, 7), dict(group=8, pads=[3, 3, 3, 3]), "depthwise", {}, 2),
+    ("f32", (2, 8, 12, 16), (8, 1, 5, 5), dict(group=8, pads=[2, 2, 2, 2]), "depthwise", {}, 2),
     ("f16", (2, 12, 5, 9, 8), (24, 3, 3, 3, 3), dict(group=4, pads=[1, 1, 1, 1, 1, 1]), "grouped",
      {}, 2),
     ("f32", (2, 16, 40), (32, 4, 5), dict(group=4, strides=[2], auto_pad="SAME_LOWER"), "grouped",
