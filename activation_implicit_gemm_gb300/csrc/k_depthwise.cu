@@ -441,7 +441,7 @@ __device__ __forceinline__ void dw_strip_store(const ConvGeom& g, const DwTileAr
 // copies into shared memory, kDwStreamAhead - 1 rows ahead of their use, so the loads are
 // in flight during the FMAs; no thread reads another's slots, so there is no barrier. The
 // loop body is one row (K*K*4 FMAs), small enough for the instruction cache. The tiled
-// kernel (below) covers the other shapes and the half2 mode.
+// kernel (below) covers the other shapes.
 template <typename T>
 struct DwVec;
 template <>
@@ -482,7 +482,7 @@ constexpr int kDwStreamAhead = 4;  // rows of X (and Z) in the ring per thread
 template <typename T, int K, int OFF>
 __host__ __device__ constexpr int dw_stream_nq() { return (OFF + K + 3 + 3) / 4; }
 
-template <typename T, int K, int OFF, int ACT>
+template <typename T, int K, int OFF, int ACT, bool H2>
 __device__ __forceinline__ void dw_stream_column(const ConvGeom& g, const T* __restrict__ x,
                                                  const T* __restrict__ w, const T* __restrict__ b,
                                                  const T* __restrict__ z, T* __restrict__ y,
@@ -491,9 +491,18 @@ __device__ __forceinline__ void dw_stream_column(const ConvGeom& g, const T* __r
   constexpr int NQ = dw_stream_nq<T, K, OFF>();
   constexpr int D = kDwStreamAhead;
   const int c = (int)(plane % g.C);
-  float wr[K * K];
+  float wr[H2 ? 1 : K * K];
+  uint32_t wh[H2 ? K * K : 1];  // half2 (w, w) per tap in the half2 mode
+  if constexpr (H2) {
 #pragma unroll
-  for (int i = 0; i < K * K; ++i) wr[i] = to_f32(w[(long long)c * K * K + i]);
+    for (int i = 0; i < K * K; ++i) {
+      const __half2 h2 = __half2half2(*reinterpret_cast<const __half*>(&w[(long long)c * K * K + i]));
+      wh[i] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < K * K; ++i) wr[i] = to_f32(w[(long long)c * K * K + i]);
+  }
   const float bias = b ? to_f32(b[c]) : 0.0f;
   const int ox = 4 * t;
   const int xs = ox - g.pW - OFF;  // column of the first vector (a multiple of 4)
@@ -536,17 +545,53 @@ __device__ __forceinline__ void dw_stream_column(const ConvGeom& g, const T* __r
     issue(r + D - 1);             // D - 1 rows ahead of this one
     ptx::cp_async_wait<D - 1>();  // this step's group has landed
     const uint32_t slot = me + (uint32_t)((r % D) * (NQ + 1)) * kStep;
-    float win[4 * NQ];
+    if constexpr (H2) {
+      // half2 row partials (the tiled kernel's arithmetic, in the same order): per slot and
+      // pair of outputs (j, j + 1), the K taps of the slot's kernel row in packed f16 FMAs,
+      // then added to the f32 accumulators
+      uint32_t wv[2 * NQ];
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) V::read(slot + (uint32_t)q * kStep, win + 4 * q);
+      for (int q = 0; q < NQ; ++q)
+        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                     : "=r"(wv[2 * q]), "=r"(wv[2 * q + 1]) : "r"(slot + (uint32_t)q * kStep));
+      uint32_t pr[K + 2];  // pr[u] = (x[OFF + u], x[OFF + u + 1])
 #pragma unroll
-    for (int kx = 0; kx < K; ++kx)
+      for (int u = 0; u < K + 2; ++u) {
+        const int s0 = OFF + u;
+        pr[u] = (s0 % 2 == 0) ? wv[s0 / 2] : prmt_b32(wv[s0 / 2], wv[s0 / 2 + 1], 0x5432u);
+      }
 #pragma unroll
       for (int sl = 0; sl < K; ++sl) {
-        const float wv = wr[(K - 1 - sl) * K + kx];
+        const int ky = K - 1 - sl;
+        __half2 p0 = __hmul2(*reinterpret_cast<const __half2*>(&pr[0]),
+                             *reinterpret_cast<const __half2*>(&wh[ky * K]));
+        __half2 p1 = __hmul2(*reinterpret_cast<const __half2*>(&pr[2]),
+                             *reinterpret_cast<const __half2*>(&wh[ky * K]));
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[sl][j] = fmaf(win[OFF + j + kx], wv, acc[sl][j]);
+        for (int kx = 1; kx < K; ++kx) {
+          const __half2 w2 = *reinterpret_cast<const __half2*>(&wh[ky * K + kx]);
+          p0 = __hfma2(*reinterpret_cast<const __half2*>(&pr[kx]), w2, p0);
+          p1 = __hfma2(*reinterpret_cast<const __half2*>(&pr[kx + 2]), w2, p1);
+        }
+        const float2 f0 = __half22float2(p0), f1 = __half22float2(p1);
+        acc[sl][0] += f0.x;
+        acc[sl][1] += f0.y;
+        acc[sl][2] += f1.x;
+        acc[sl][3] += f1.y;
       }
+    } else {
+      float win[4 * NQ];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) V::read(slot + (uint32_t)q * kStep, win + 4 * q);
+#pragma unroll
+      for (int kx = 0; kx < K; ++kx)
+#pragma unroll
+        for (int sl = 0; sl < K; ++sl) {
+          const float wv = wr[(K - 1 - sl) * K + kx];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[sl][j] = fmaf(win[OFF + j + kx], wv, acc[sl][j]);
+        }
+    }
     const int o = r - (K - 1);  // the output row slot 0 completes now
     if (o >= 0) {
       float zv[4];
@@ -567,7 +612,7 @@ __device__ __forceinline__ void dw_stream_column(const ConvGeom& g, const T* __r
   ptx::cp_async_wait<0>();  // the ring's last (empty) groups, before the slots are reused
 }
 
-template <typename T, int K, int OFF>
+template <typename T, int K, int OFF, bool H2>
 __global__ void __launch_bounds__(kDwStreamThreads, 1)
     dw_stream_kernel(const ConvGeom g, int tpp, long long nthr, const T* __restrict__ x,
                      const T* __restrict__ w, const T* __restrict__ b, const T* __restrict__ z,
@@ -580,7 +625,7 @@ __global__ void __launch_bounds__(kDwStreamThreads, 1)
   for (long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x; gid < nthr; gid += stride) {
     const long long plane = gid / tpp;
     const int t = (int)(gid - plane * tpp);
-#define FCONV_DW_STREAM(ACT) dw_stream_column<T, K, OFF, ACT>(g, x, w, b, z, y, plane, t, ring)
+#define FCONV_DW_STREAM(ACT) dw_stream_column<T, K, OFF, ACT, H2>(g, x, w, b, z, y, plane, t, ring)
     FCONV_ACT_SWITCH(g.act, FCONV_DW_STREAM)
 #undef FCONV_DW_STREAM
   }
@@ -901,13 +946,15 @@ __global__ void __launch_bounds__(kDwThreads) dw_kernel_generic(ConvGeom g, cons
 // The column-streaming kernel takes stride 1, dilation 1, K in {3, 5, 7} with the left pad
 // of a same-size conv modulo 4 ((K - 1) / 2, so that one vector offset per K is compiled),
 // rows of X and Y that are whole 4-element vectors, and vector-aligned X, Z and Y, in the
-// default precision.
+// default precision or (f16) the half2 mode.
 bool dw_stream_ok(const ConvGeom& g) {
   if (!(g.Cg == 1 && g.Mg == 1 && g.KD == 1 && g.ID == 1 && g.OD == 1)) return false;
   if (!(g.sW == 1 && g.dW == 1 && g.sH == 1 && g.dH == 1 && g.KH == g.KW)) return false;
   if (g.KW != 3 && g.KW != 5 && g.KW != 7) return false;
   if ((g.pW - (g.KW - 1) / 2) % 4 != 0) return false;
-  if (g.precision != FCONV_PRECISION_DEFAULT) return false;
+  if (g.precision != FCONV_PRECISION_DEFAULT &&
+      !(g.precision == FCONV_PRECISION_HALF2_ROWS && g.dtype == FCONV_F16))
+    return false;
   if (g.N < 1 || g.C < 1 || g.OH < 1 || g.OW < 4) return false;
   return g.IW % 4 == 0 && g.OW % 4 == 0 && (long long)g.N * g.C * (g.OW / 4) < 0x7fffffffLL * 128LL;
 }
@@ -925,9 +972,10 @@ int launch_dw_stream(const ConvGeom& g, const ConvArgs& a, cudaStream_t s) {
   if (grid > sms) grid = sms;
   if (g.max_ctas > 0 && grid > g.max_ctas) grid = g.max_ctas;
   const int off = ((-g.pW) % 4 + 4) % 4;
+  const bool h2 = g.precision == FCONV_PRECISION_HALF2_ROWS;
 #define FCONV_DW_STREAM_K(KV, OV)                                                              \
   if (g.KW == KV && off == OV) {                                                               \
-    auto k = dw_stream_kernel<T, KV, OV>;                                                      \
+    auto k = h2 ? dw_stream_kernel<T, KV, OV, sizeof(T) == 2> : dw_stream_kernel<T, KV, OV, false>; \
     const size_t smem = (size_t)kDwStreamAhead * (dw_stream_nq<T, KV, OV>() + 1) *             \
                         kDwStreamThreads * DwVec<T>::bytes;                                    \
     const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,  \

@@ -219,8 +219,8 @@ def tf32x3_peak(peaks):
 def dw_streams(case, plan) -> bool:
     """Whether a depthwise plan runs the column-streaming kernel: 2-D, stride 1, dilation 1,
     K in {3, 5, 7}, the same-size left pad modulo 4, rows of X and Y in whole 4-element
-    vectors, default precision (the library's rule; the bench's buffers are aligned)."""
-    if len(case.x_shape) != 4 or getattr(plan, "precision", "default") != "default":
+    vectors (the library's rule, in either precision; the bench's buffers are aligned)."""
+    if len(case.x_shape) != 4:
         return False
     k = case.w_shape[-1]
     ones = lambda v: v is None or all(e == 1 for e in v)
@@ -304,7 +304,7 @@ def measure_next_rows(dev, stream, flush, peaks):
                  "frac_of_hbm": round(plan.bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                  "default_precision_us": round(times["default"][1] * 1e3, 2),
                  "speedup_vs_default": round(times["default"][1] / ms, 3),
-                 "kernel": "dw_tile_kernel<__half, 7, 7, true>",
+                 "kernel": "dw_stream_kernel<__half, 7, 1, true>",
                  "error": "bounded by f16 rounding + 7 * 2^-11 * sum|x*w| (tests/test_gpu_half2.py)"})
     for case in workloads.PATCHIFY_CASES:
         y_shape = fc.FusedConvPlan(_lib.F16, case.x_shape, case.w_shape, has_bias=case.has_bias,
