@@ -4,11 +4,17 @@
 // vector per thread, bias seeding the accumulators, f32 accumulation) restated for
 // GB300.
 //
-// One CTA per (image, channel, band of output rows). The CTA stages the band's input
-// rows, zero-padded left/right/top/bottom, in shared memory as fp32; each thread then
-// produces runs of VW consecutive outputs of one row from a register window of
-// VW + KW - 1 input values per kernel row; bias, residual Z, the activation and the
-// cast to T are applied before the store.
+// Kernels, in the order the host picks them (launch_dw_t):
+//   dw_stream_kernel   stride 1, K in {3, 5, 7}, the same-size left pad, rows of X and Y in
+//                      whole 4-element vectors: a thread walks 4 output columns down a
+//                      whole plane with K rolling accumulator rows (see its comment)
+//   dw_tile_kernel     other stride-1 shapes whose X rows TMA can address: persistent,
+//                      TMA-staged tiles, TH-row register strips
+//   dw_kernel_block    other stride-1 shapes with K in {3, 5, 7}
+//   dw_kernel_generic  any stride and dilation: one CTA per (image, channel, band of output
+//                      rows) stages the band's input rows, zero-padded, in shared memory as
+//                      fp32; each thread makes one output at a time
+// All apply bias, residual Z, the activation and the cast to T before the store.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
