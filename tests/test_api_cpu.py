@@ -315,3 +315,30 @@ def test_half2_precision_is_depthwise_f16_only(lib):
         with pytest.raises(FconvError) as e:
             FusedConvPlan(dt, xs, ws, precision="half2_rows", **attrs)
         assert e.value.code == "E_UNSUPPORTED"
+
+
+def test_bench_names_the_depthwise_kernel(lib):
+    """The bench report names the streaming depthwise kernel exactly for the shapes the
+    library streams (stride 1, K in 3/5/7, the same-size left pad modulo 4, X and Y rows in
+    whole 4-element vectors), in either precision, and the tiled kernel otherwise."""
+    import importlib.util
+    import os
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    spec = importlib.util.spec_from_file_location("bench_names", os.path.join(root, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+
+    def name(xs, k, precision="default", **attrs):
+        case = workloads.ConvCase("t", "f16", xs, (xs[1], 1, k, k), group=xs[1], **attrs)
+        p = FusedConvPlan(_lib.F16, xs, case.w_shape, precision=precision, **case.attrs())
+        return bench.main_kernel_name(case, p.route, p)
+
+    stem = workloads.case_by_name("stem_dw_128_k7")
+    assert name(stem.x_shape, 7, pads=(3, 3, 3, 3)) == "dw_stream_kernel"
+    assert name(stem.x_shape, 7, precision="half2_rows", pads=(3, 3, 3, 3)) == "dw_stream_kernel"
+    assert name((2, 8, 16, 16), 3, pads=(1, 1, 1, 1)) == "dw_stream_kernel"
+    assert name((2, 8, 16, 16), 7, pads=(7, 7, 7, 7)) == "dw_stream_kernel"   # 7 = 3 mod 4
+    assert name((2, 8, 16, 24), 5, auto_pad="SAME_UPPER") == "dw_stream_kernel"
+    assert name((2, 8, 16, 21), 3, pads=(1, 1, 1, 1)) == "dw_tile_kernel"     # X rows ragged
+    assert name((2, 8, 16, 24), 7, pads=(3, 0, 3, 0)) == "dw_tile_kernel"     # left pad 0
+    assert name((2, 8, 16, 16), 3, pads=(1, 1, 1, 2)) == "dw_tile_kernel"     # Y rows ragged
